@@ -1,0 +1,172 @@
+/*
+ * swa.h -- C ABI of the sliding-window attention library (libswa.so, sm_103a).
+ *
+ * Operations
+ * ----------
+ * swa_fwd     Prefill / encoder attention over a band:
+ *               o_t = sum over allowed s of softmax_s(scale * q_t . k_s) v_s
+ *             Allowed keys of query t: window_left / window_right bound the band
+ *             t - window_left <= s <= t + window_right (a negative value leaves that
+ *             side unbounded), clipped to [0, T).  The causal window of W keys,
+ *             N_t = [max(0, t-W+1), t] (Sliding Window Attention,
+ *             lizeman.github.io llm-arch-kb, section 2 "Derivation"), is
+ *             window_left = W-1, window_right = 0.  The bidirectional window
+ *             |t - s| <= r (prathamp.com "Sliding Window Attention: From Local
+ *             Windows to Global Context", section 1.1) is window_left =
+ *             window_right = r.  Global positions (same page, section 4.3) attend
+ *             to every key and are attended by every query; a global key already
+ *             inside a query's band is counted once.
+ * swa_decode  One query token per sequence against a ring-buffer KV cache of W
+ *             slots.  Token p is stored in slot p mod W (lizeman page, KV cache
+ *             paragraph) and every slot carries its true token position; the
+ *             window is evaluated on positions, not slot offsets (Gemma 3 note,
+ *             ai-engineer-exhaustive.pages.dev, "How it works"): slot j is attended
+ *             by the query at position t iff 0 <= pos_j and t - W < pos_j <= t.
+ *
+ * Conventions
+ * -----------
+ * - Element types: q, k, v, o are bf16; lse is fp32 (natural log of the softmax
+ *   normaliser of the scaled scores, i.e. lse_t = log sum_s exp(scale q_t . k_s));
+ *   row_counts are int32 numbers of attended keys.
+ * - Grouped-query attention: H_q must be a multiple of H_kv; query head h reads
+ *   key/value head h / (H_q / H_kv).
+ * - Ownership: every pointer is device memory owned by the caller (unless stated
+ *   otherwise); the library allocates nothing and keeps no pointer after return.
+ * - Asynchrony: work is enqueued on `stream` and the call returns without
+ *   synchronising.  Argument errors are detected on the host and returned before
+ *   anything is launched.  SWA_ERR_CUDA reports a failed launch.
+ * - Bounded waits: every wait inside a kernel has a time limit; on expiry the
+ *   kernel records an error word in device memory and returns.  The word is
+ *   read (and cleared) by swa_check_device_error().
+ * - Thread safety: calls may be made from several host threads on different
+ *   streams; workspaces must not be shared between calls that overlap in time.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SWA_API __attribute__((visibility("default")))
+#else
+#define SWA_API
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *swa_stream_t;
+
+typedef enum swa_status {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, stride or window */
+    SWA_ERR_UNSUPPORTED = 2, /* valid but not built: head dim, group size, alignment */
+    SWA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    SWA_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (see swa_check_device_error) */
+    SWA_ERR_WORKSPACE = 5    /* workspace null or smaller than the *_workspace_size answer */
+} swa_status;
+
+/*
+ * swa_fwd parameters.
+ *   q           bf16 [B, T, H_q, d_h]; q_strides = element strides of (b, t, h); d_h contiguous.
+ *   k, v        bf16 [B, T, H_kv, d_h]; k_strides / v_strides likewise.
+ *   o           bf16 [B, T, H_q, d_h]; o_strides likewise.
+ *   lse         fp32 [B, H_q, T], contiguous.
+ *   row_counts  optional int32 [B, H_q, T], contiguous (NULL: not written).
+ *   global_idx  optional int32 [n_global] device array of global positions, strictly
+ *               increasing, each in [0, T) (NULL with n_global = 0: none).
+ * Requirements: d_h in {64, 128, 256}; H_q % H_kv == 0 and H_q / H_kv <= 16;
+ * every base pointer 16-byte aligned; strides multiples of 8 elements; T >= 1.
+ */
+typedef struct swa_fwd_params {
+    const void *q;
+    const void *k;
+    const void *v;
+    int64_t q_strides[3];
+    int64_t k_strides[3];
+    int64_t v_strides[3];
+    int32_t B, T, H_q, H_kv, d_h;
+    int32_t window_left;
+    int32_t window_right;
+    float scale;
+    const int32_t *global_idx;
+    int32_t n_global;
+    void *o;
+    int64_t o_strides[3];
+    float *lse;
+    int32_t *row_counts;
+} swa_fwd_params;
+
+/* Bytes of device workspace swa_fwd needs (0 when n_global == 0); 0 for invalid params. */
+SWA_API size_t swa_fwd_workspace_size(const swa_fwd_params *p);
+
+/*
+ * Banded attention (plus global rows and columns).  workspace: device memory of at
+ * least swa_fwd_workspace_size(p) bytes, 256-byte aligned (may be NULL when that is 0).
+ * Errors: SWA_ERR_INVALID_ARG / SWA_ERR_UNSUPPORTED / SWA_ERR_WORKSPACE before any
+ * launch; SWA_ERR_CUDA if a launch fails.
+ */
+SWA_API swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_bytes,
+                   swa_stream_t stream);
+
+/*
+ * swa_decode parameters (all contiguous).
+ *   q          bf16 [B, H_q, d_h]    the current token's queries
+ *   k_cache    bf16 [B, H_kv, W, d_h] ring buffers (the current token already stored)
+ *   v_cache    bf16 [B, H_kv, W, d_h]
+ *   slot_pos   int32 [B, W]  true token position held by each slot (< 0: never written)
+ *   q_pos      int32 [B]     position t_b of the current token
+ *   o          bf16 [B, H_q, d_h]
+ *   lse        fp32 [B, H_q]
+ *   row_counts optional int32 [B, H_q]
+ * Requirements: d_h in {64, 128, 256}; H_q % H_kv == 0 and H_q / H_kv <= 16; W >= 1;
+ * pointers 16-byte aligned.
+ */
+typedef struct swa_decode_params {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *slot_pos;
+    const int32_t *q_pos;
+    int32_t B, H_q, H_kv, d_h, W;
+    float scale;
+    void *o;
+    float *lse;
+    int32_t *row_counts;
+} swa_decode_params;
+
+/* Bytes of device workspace swa_decode needs (split partials); 0 for invalid params. */
+SWA_API size_t swa_decode_workspace_size(const swa_decode_params *p);
+
+/*
+ * Split-K decode: the W slots are cut into splits scored in parallel, each split
+ * keeps a running (max, sum, weighted values) triple, and a second kernel merges
+ * the splits by log-sum-exp.  workspace: >= swa_decode_workspace_size(p) bytes,
+ * 256-byte aligned.  Errors as for swa_fwd.
+ */
+SWA_API swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error words.
+ * Returns SWA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, SWA_ERR_CUDA if the synchronisation failed, else SWA_OK.
+ */
+SWA_API swa_status swa_check_device_error(swa_stream_t stream);
+
+/* Static description of a status code. */
+SWA_API const char *swa_status_string(swa_status s);
+
+/* ABI version of this header (incremented on any layout change). */
+SWA_API int32_t swa_abi_version(void);
+
+#define SWA_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,246 @@
+"""Sliding-window attention on GB300 (sm_103a): thin Python binding of libswa.so.
+
+The functions here marshal torch tensors into the C ABI of ``include/swa.h``
+(``swa_fwd``, ``swa_decode`` and their workspace queries) and call it on the
+current CUDA stream.  Every step of the computation runs in the library's
+kernels; there is no fallback path.  If the library has not been built, the
+first call raises (``build()`` compiles it in-tree with nvcc).
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build_mod
+
+__all__ = [
+    "SwaError", "build", "load_library", "library_path",
+    "swa_fwd", "swa_decode", "swa_fwd_workspace_size", "swa_decode_workspace_size",
+    "swa_check_device_error", "swa_status_string", "swa_abi_version",
+    "SwaFwdParams", "SwaDecodeParams",
+]
+
+_c_i64x3 = ctypes.c_int64 * 3
+
+
+class SwaFwdParams(ctypes.Structure):
+    """Mirror of ``swa_fwd_params`` in include/swa.h."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_strides", _c_i64x3), ("k_strides", _c_i64x3), ("v_strides", _c_i64x3),
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+        ("d_h", ctypes.c_int32), ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("global_idx", ctypes.c_void_p), ("n_global", ctypes.c_int32),
+        ("o", ctypes.c_void_p), ("o_strides", _c_i64x3), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p),
+    ]
+
+
+class SwaDecodeParams(ctypes.Structure):
+    """Mirror of ``swa_decode_params`` in include/swa.h."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("slot_pos", ctypes.c_void_p), ("q_pos", ctypes.c_void_p),
+        ("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
+        ("W", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p),
+    ]
+
+
+STATUS = {0: "SWA_OK", 1: "SWA_ERR_INVALID_ARG", 2: "SWA_ERR_UNSUPPORTED", 3: "SWA_ERR_CUDA",
+          4: "SWA_ERR_TIMEOUT", 5: "SWA_ERR_WORKSPACE"}
+
+
+class SwaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}: {swa_status_string(status)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build_mod.LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile libswa.so for sm_103a (in-tree) and return its path."""
+    return _build_mod.build(force=force)
+
+
+def load_library(path: str | None = None):
+    """Load libswa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"libswa.so not found at {p}; call sliding_window_attention_swa_gb300.build() first")
+    lib = ctypes.CDLL(p)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.swa_fwd_workspace_size.argtypes = [ctypes.POINTER(SwaFwdParams)]
+    lib.swa_fwd_workspace_size.restype = sz
+    lib.swa_fwd.argtypes = [ctypes.POINTER(SwaFwdParams), vp, sz, vp]
+    lib.swa_fwd.restype = ctypes.c_int
+    lib.swa_decode_workspace_size.argtypes = [ctypes.POINTER(SwaDecodeParams)]
+    lib.swa_decode_workspace_size.restype = sz
+    lib.swa_decode.argtypes = [ctypes.POINTER(SwaDecodeParams), vp, sz, vp]
+    lib.swa_decode.restype = ctypes.c_int
+    lib.swa_check_device_error.argtypes = [vp]
+    lib.swa_check_device_error.restype = ctypes.c_int
+    lib.swa_status_string.argtypes = [ctypes.c_int]
+    lib.swa_status_string.restype = ctypes.c_char_p
+    lib.swa_abi_version.argtypes = []
+    lib.swa_abi_version.restype = ctypes.c_int32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def swa_status_string(status: int) -> str:
+    return load_library().swa_status_string(int(status)).decode()
+
+
+def swa_abi_version() -> int:
+    return int(load_library().swa_abi_version())
+
+
+def _stream_handle(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_bf16(name, t, ndim):
+    import torch
+
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != ndim or t.stride(-1) != 1:
+        raise ValueError(f"{name}: expected a CUDA bf16 tensor of rank {ndim} with a contiguous last dim")
+
+
+def fwd_params(q, k, v, window_left: int, window_right: int, scale: float, global_idx, o, lse, row_counts):
+    """Fill a SwaFwdParams from tensors (q/k/v/o [B,T,H,d] bf16; lse/row_counts [B,H_q,T])."""
+    B, T, Hq, D = q.shape
+    p = SwaFwdParams()
+    p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    p.q_strides = _c_i64x3(*q.stride()[:3])
+    p.k_strides = _c_i64x3(*k.stride()[:3])
+    p.v_strides = _c_i64x3(*v.stride()[:3])
+    p.o_strides = _c_i64x3(*o.stride()[:3])
+    p.B, p.T, p.H_q, p.H_kv, p.d_h = B, T, Hq, k.shape[2], D
+    p.window_left, p.window_right = int(window_left), int(window_right)
+    p.scale = float(scale)
+    p.global_idx = None if global_idx is None else global_idx.data_ptr()
+    p.n_global = 0 if global_idx is None else int(global_idx.numel())
+    p.lse = lse.data_ptr()
+    p.row_counts = None if row_counts is None else row_counts.data_ptr()
+    return p
+
+
+def swa_fwd_workspace_size(params: SwaFwdParams) -> int:
+    return int(load_library().swa_fwd_workspace_size(ctypes.byref(params)))
+
+
+def swa_fwd(q, k, v, window_left: int, window_right: int, scale: float | None = None, global_idx=None, *,
+            o=None, lse=None, row_counts=None, want_counts: bool = False, workspace=None, stream=None):
+    """Banded attention over q [B,T,H_q,d], k/v [B,T,H_kv,d] (bf16, CUDA).
+
+    Keys s with t - window_left <= s <= t + window_right (negative: unbounded side),
+    plus global positions (int32 CUDA tensor, strictly increasing).  Returns
+    (o [B,T,H_q,d] bf16, lse [B,H_q,T] fp32, row_counts [B,H_q,T] int32 or None).
+    """
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(name, t, 4)
+    B, T, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    if global_idx is not None:
+        if global_idx.dtype != torch.int32 or not global_idx.is_cuda:
+            raise ValueError("global_idx: expected a CUDA int32 tensor")
+        global_idx = global_idx.contiguous()
+        if global_idx.numel() == 0:
+            global_idx = None
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    if row_counts is None and want_counts:
+        row_counts = torch.empty((B, Hq, T), dtype=torch.int32, device=q.device)
+    p = fwd_params(q, k, v, window_left, window_right, scale, global_idx, o, lse, row_counts)
+    need = int(lib.swa_fwd_workspace_size(ctypes.byref(p)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.swa_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_fwd", st)
+    return o, lse, row_counts
+
+
+def decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale: float, o, lse, row_counts):
+    B, Hq, D = q.shape
+    p = SwaDecodeParams()
+    p.q, p.k_cache, p.v_cache = q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr()
+    p.slot_pos, p.q_pos = slot_pos.data_ptr(), q_pos.data_ptr()
+    p.B, p.H_q, p.H_kv, p.d_h, p.W = B, Hq, k_cache.shape[1], D, k_cache.shape[2]
+    p.scale = float(scale)
+    p.o, p.lse = o.data_ptr(), lse.data_ptr()
+    p.row_counts = None if row_counts is None else row_counts.data_ptr()
+    return p
+
+
+def swa_decode_workspace_size(params: SwaDecodeParams) -> int:
+    return int(load_library().swa_decode_workspace_size(ctypes.byref(params)))
+
+
+def swa_decode(q, k_cache, v_cache, slot_pos, q_pos, scale: float | None = None, *, o=None, lse=None,
+               row_counts=None, want_counts: bool = False, workspace=None, stream=None):
+    """Ring-buffer decode: q [B,H_q,d], caches [B,H_kv,W,d] (bf16), slot_pos [B,W], q_pos [B] (int32).
+
+    Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32, row_counts [B,H_q] int32 or None).
+    """
+    import torch
+
+    lib = load_library()
+    _check_bf16("q", q, 3)
+    _check_bf16("k_cache", k_cache, 4)
+    _check_bf16("v_cache", v_cache, 4)
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("slot_pos", slot_pos), ("q_pos", q_pos)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+    if slot_pos.dtype != torch.int32 or q_pos.dtype != torch.int32:
+        raise ValueError("slot_pos and q_pos must be int32")
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if row_counts is None and want_counts:
+        row_counts = torch.empty((B, Hq), dtype=torch.int32, device=q.device)
+    p = decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale, o, lse, row_counts)
+    need = int(lib.swa_decode_workspace_size(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.swa_decode(ctypes.byref(p), _ptr(workspace), ws_bytes, _stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_decode", st)
+    return o, lse, row_counts
+
+
+def swa_check_device_error(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel gave up on a bounded wait."""
+    st = load_library().swa_check_device_error(_stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_check_device_error", st)

@@ -1,0 +1,256 @@
+// swa_abi.cu -- the extern "C" entry points of libswa.so: argument validation on
+// the host, workspace sizing, and the kernel launches on the caller's stream.
+#include <cmath>
+#include <cstdint>
+
+#include "swa_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+bool strides_ok(const int64_t st[3]) {
+    for (int i = 0; i < 3; ++i)
+        if (st[i] <= 0 || (st[i] % 8) != 0) return false;
+    return true;
+}
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+constexpr float kLog2e = 1.4426950408889634f;
+
+swa_status fwd_check(const swa_fwd_params *p) {
+    if (!p || !p->q || !p->k || !p->v || !p->o || !p->lse) return SWA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->T < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1) return SWA_ERR_INVALID_ARG;
+    if (p->H_q % p->H_kv != 0) return SWA_ERR_INVALID_ARG;
+    if (p->n_global < 0 || p->n_global > p->T) return SWA_ERR_INVALID_ARG;
+    if (p->n_global > 0 && !p->global_idx) return SWA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
+    if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
+    if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
+    if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
+    if (!strides_ok(p->q_strides) || !strides_ok(p->k_strides) || !strides_ok(p->v_strides) ||
+        !strides_ok(p->o_strides))
+        return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o) ||
+        (p->global_idx && (reinterpret_cast<uintptr_t>(p->global_idx) & 3u)) ||
+        (reinterpret_cast<uintptr_t>(p->lse) & 3u) || (reinterpret_cast<uintptr_t>(p->row_counts) & 3u))
+        return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+swa_status decode_check(const swa_decode_params *p) {
+    if (!p || !p->q || !p->k_cache || !p->v_cache || !p->slot_pos || !p->q_pos || !p->o || !p->lse)
+        return SWA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1 || p->W < 1) return SWA_ERR_INVALID_ARG;
+    if (p->H_q % p->H_kv != 0) return SWA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
+    if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
+    if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
+    if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(p->q) || !aligned16(p->k_cache) || !aligned16(p->v_cache) || !aligned16(p->o) ||
+        (reinterpret_cast<uintptr_t>(p->slot_pos) & 3u) || (reinterpret_cast<uintptr_t>(p->q_pos) & 3u) ||
+        (reinterpret_cast<uintptr_t>(p->lse) & 3u) || (reinterpret_cast<uintptr_t>(p->row_counts) & 3u))
+        return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+swa_status workspace_ok(void *ws, size_t have, size_t need) {
+    if (need == 0) return SWA_OK;
+    if (!ws || have < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SWA_ERR_WORKSPACE;
+    return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t swa_abi_version(void) { return SWA_ABI_VERSION; }
+
+const char *swa_status_string(swa_status s) {
+    switch (s) {
+        case SWA_OK: return "ok";
+        case SWA_ERR_INVALID_ARG: return "invalid argument";
+        case SWA_ERR_UNSUPPORTED: return "unsupported configuration (head dim, group size, scale or alignment)";
+        case SWA_ERR_CUDA: return "CUDA launch or runtime error";
+        case SWA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+        case SWA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    }
+    return "unknown status";
+}
+
+size_t swa_fwd_workspace_size(const swa_fwd_params *p) {
+    if (fwd_check(p) != SWA_OK || p->n_global == 0) return 0;
+    return swa::split_workspace_bytes(p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T);
+}
+
+swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_bytes, swa_stream_t stream) {
+    swa_status st = fwd_check(p);
+    if (st != SWA_OK) return st;
+    st = workspace_ok(workspace, workspace_bytes, swa_fwd_workspace_size(p));
+    if (st != SWA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float scale_log2 = p->scale * kLog2e;
+
+    swa::BandArgs ba{};
+    ba.q = p->q;
+    ba.k = p->k;
+    ba.v = p->v;
+    ba.o = p->o;
+    for (int i = 0; i < 3; ++i) {
+        ba.q_st[i] = p->q_strides[i];
+        ba.k_st[i] = p->k_strides[i];
+        ba.v_st[i] = p->v_strides[i];
+        ba.o_st[i] = p->o_strides[i];
+    }
+    ba.B = p->B;
+    ba.T = p->T;
+    ba.H_q = p->H_q;
+    ba.H_kv = p->H_kv;
+    ba.D = p->d_h;
+    ba.wl = p->window_left < 0 ? -1 : p->window_left;
+    ba.wr = p->window_right < 0 ? -1 : p->window_right;
+    ba.scale_log2 = scale_log2;
+    ba.global_idx = p->n_global > 0 ? p->global_idx : nullptr;
+    ba.n_global = p->n_global;
+    ba.lse = p->lse;
+    ba.counts = p->row_counts;
+    if (swa::launch_band(ba, s) != cudaSuccess) return SWA_ERR_CUDA;
+
+    if (p->n_global > 0) {
+        // Global rows attend to all T keys: split-K over T, merged by log-sum-exp,
+        // overwriting the rows the band kernel wrote for those positions.
+        swa::SplitArgs sa{};
+        sa.q = p->q;
+        sa.q_sb = p->q_strides[0];
+        sa.q_st = p->q_strides[1];
+        sa.q_sh = p->q_strides[2];
+        sa.k = p->k;
+        sa.v = p->v;
+        sa.k_sb = p->k_strides[0];
+        sa.k_ss = p->k_strides[1];
+        sa.k_sh = p->k_strides[2];
+        sa.v_sb = p->v_strides[0];
+        sa.v_ss = p->v_strides[1];
+        sa.v_sh = p->v_strides[2];
+        sa.slot_pos = nullptr;
+        sa.q_pos = nullptr;
+        sa.q_tok = p->global_idx;
+        sa.tok_limit = p->T;
+        sa.B = p->B;
+        sa.NQ = p->n_global;
+        sa.H_q = p->H_q;
+        sa.H_kv = p->H_kv;
+        sa.D = p->d_h;
+        sa.n_slots = p->T;
+        sa.W = p->T;
+        sa.scale_log2 = scale_log2;
+        sa.slots_per_split = swa::kSlotsPerSplit;
+        sa.n_splits = swa::split_count(p->T);
+        sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
+        swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T, &sa.ws_ml, &sa.ws_acc,
+                         &sa.ws_cnt);
+        if (swa::launch_split(sa, s) != cudaSuccess) return SWA_ERR_CUDA;
+        swa::MergeArgs ma{};
+        ma.ws_ml = sa.ws_ml;
+        ma.ws_acc = sa.ws_acc;
+        ma.ws_cnt = sa.ws_cnt;
+        ma.B = p->B;
+        ma.NQ = p->n_global;
+        ma.H_q = p->H_q;
+        ma.H_kv = p->H_kv;
+        ma.D = p->d_h;
+        ma.n_splits = sa.n_splits;
+        ma.q_tok = p->global_idx;
+        ma.tok_limit = p->T;
+        ma.o = p->o;
+        ma.o_sb = p->o_strides[0];
+        ma.o_st = p->o_strides[1];
+        ma.o_sh = p->o_strides[2];
+        ma.lse = p->lse;
+        ma.lse_sb = static_cast<int64_t>(p->H_q) * p->T;
+        ma.lse_sh = p->T;
+        ma.lse_st = 1;
+        ma.counts = p->row_counts;
+        ma.cnt_sb = ma.lse_sb;
+        ma.cnt_sh = ma.lse_sh;
+        ma.cnt_st = 1;
+        if (swa::launch_merge(ma, s) != cudaSuccess) return SWA_ERR_CUDA;
+    }
+    return SWA_OK;
+}
+
+size_t swa_decode_workspace_size(const swa_decode_params *p) {
+    if (decode_check(p) != SWA_OK) return 0;
+    return swa::split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, p->W);
+}
+
+swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t workspace_bytes, swa_stream_t stream) {
+    swa_status st = decode_check(p);
+    if (st != SWA_OK) return st;
+    st = workspace_ok(workspace, workspace_bytes, swa_decode_workspace_size(p));
+    if (st != SWA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t D = p->d_h, W = p->W;
+
+    swa::SplitArgs sa{};
+    sa.q = p->q;
+    sa.q_sb = static_cast<int64_t>(p->H_q) * D;
+    sa.q_st = 0;
+    sa.q_sh = D;
+    sa.k = p->k_cache;
+    sa.v = p->v_cache;
+    sa.k_sb = sa.v_sb = static_cast<int64_t>(p->H_kv) * W * D;
+    sa.k_ss = sa.v_ss = D;
+    sa.k_sh = sa.v_sh = W * D;
+    sa.slot_pos = p->slot_pos;
+    sa.q_pos = p->q_pos;
+    sa.q_tok = nullptr;
+    sa.tok_limit = 1;
+    sa.B = p->B;
+    sa.NQ = 1;
+    sa.H_q = p->H_q;
+    sa.H_kv = p->H_kv;
+    sa.D = p->d_h;
+    sa.n_slots = p->W;
+    sa.W = p->W;
+    sa.scale_log2 = p->scale * kLog2e;
+    sa.slots_per_split = swa::kSlotsPerSplit;
+    sa.n_splits = swa::split_count(p->W);
+    sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
+    swa::split_carve(workspace, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
+    if (swa::launch_split(sa, s) != cudaSuccess) return SWA_ERR_CUDA;
+
+    swa::MergeArgs ma{};
+    ma.ws_ml = sa.ws_ml;
+    ma.ws_acc = sa.ws_acc;
+    ma.ws_cnt = sa.ws_cnt;
+    ma.B = p->B;
+    ma.NQ = 1;
+    ma.H_q = p->H_q;
+    ma.H_kv = p->H_kv;
+    ma.D = p->d_h;
+    ma.n_splits = sa.n_splits;
+    ma.q_tok = nullptr;
+    ma.tok_limit = 1;
+    ma.o = p->o;
+    ma.o_sb = static_cast<int64_t>(p->H_q) * D;
+    ma.o_st = 0;
+    ma.o_sh = D;
+    ma.lse = p->lse;
+    ma.lse_sb = p->H_q;
+    ma.lse_sh = 1;
+    ma.lse_st = 0;
+    ma.counts = p->row_counts;
+    ma.cnt_sb = p->H_q;
+    ma.cnt_sh = 1;
+    ma.cnt_st = 0;
+    if (swa::launch_merge(ma, s) != cudaSuccess) return SWA_ERR_CUDA;
+    return SWA_OK;
+}
+
+swa_status swa_check_device_error(swa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SWA_ERR_CUDA;
+    const unsigned int e = swa::band_read_clear_error();
+    return e ? SWA_ERR_TIMEOUT : SWA_OK;
+}
+
+}  // extern "C"

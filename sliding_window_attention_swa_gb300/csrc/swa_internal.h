@@ -1,0 +1,101 @@
+// swa_internal.h -- host-side interface between the C ABI (swa_abi.cu) and the
+// kernel translation units.  Not installed; the public surface is include/swa.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "swa.h"
+
+namespace swa {
+
+// One query row set attended against a list of key/value "slots".
+//   decode:      slots are the W ring-buffer slots, a slot is valid iff its stored
+//                position p satisfies 0 <= p and t - W < p <= t (t = q_pos[b]);
+//   global rows: slots are the T key positions, all valid; the queries are the
+//                rows of the global positions (q_tok[qs]).
+// Rows packed into one CTA: q_per_cta query tokens x the H_q/H_kv heads of a group.
+struct SplitArgs {
+    const void *q;
+    int64_t q_sb, q_st, q_sh;  // query element address: b*q_sb + tok*q_st + h*q_sh
+    const void *k;
+    const void *v;
+    int64_t k_sb, k_ss, k_sh;     // key element address: b*k_sb + slot*k_ss + kvh*k_sh
+    int64_t v_sb, v_ss, v_sh;     // value element address, likewise
+    const int32_t *slot_pos;      // [B, W] (decode) or nullptr (every slot < n_slots valid)
+    const int32_t *q_pos;         // [B] (decode) or nullptr
+    const int32_t *q_tok;         // [NQ] token of each query (global rows) or nullptr (token 0)
+    int tok_limit;                // q_tok entries outside [0, tok_limit) are skipped
+    int B, NQ, H_q, H_kv, D;
+    int n_slots;  // W (decode) or T (global rows)
+    int W;        // window for the position test (decode)
+    float scale_log2;
+    int slots_per_split, n_splits, q_per_cta;
+    float *ws_ml;     // [B, NQ, H_q, n_splits, 2]   (max in log2 units, sum)
+    float *ws_acc;    // [B, NQ, H_q, n_splits, D]   unnormalised weighted values
+    int32_t *ws_cnt;  // [B, H_kv, n_splits]         valid slots per split
+};
+
+struct MergeArgs {
+    const float *ws_ml;
+    const float *ws_acc;
+    const int32_t *ws_cnt;
+    int B, NQ, H_q, H_kv, D, n_splits;
+    const int32_t *q_tok;  // as in SplitArgs
+    int tok_limit;
+    void *o;
+    int64_t o_sb, o_st, o_sh;
+    float *lse;
+    int64_t lse_sb, lse_sh, lse_st;
+    int32_t *counts;  // may be nullptr
+    int64_t cnt_sb, cnt_sh, cnt_st;
+};
+
+// Split geometry shared by the workspace-size query and the launch.
+constexpr int kSplitChunk = 64;         // slots per pipeline stage
+constexpr int kSlotsPerSplit = 512;     // slots per CTA
+constexpr int kSplitRows = 16;          // mma.sync M: query rows per CTA
+
+inline int split_q_per_cta(int group) { return group >= kSplitRows ? 1 : kSplitRows / group; }
+inline int split_count(int n_slots) { return (n_slots + kSlotsPerSplit - 1) / kSlotsPerSplit; }
+inline size_t split_workspace_bytes(int B, int NQ, int H_q, int H_kv, int D, int n_slots) {
+    const size_t ns = static_cast<size_t>(split_count(n_slots));
+    const size_t rows = static_cast<size_t>(B) * NQ * H_q * ns;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    return up(rows * 2 * sizeof(float)) + up(rows * D * sizeof(float)) +
+           up(static_cast<size_t>(B) * H_kv * ns * sizeof(int32_t));
+}
+inline void split_carve(void *ws, int B, int NQ, int H_q, int H_kv, int D, int n_slots, float **ml, float **acc,
+                        int32_t **cnt) {
+    const size_t ns = static_cast<size_t>(split_count(n_slots));
+    const size_t rows = static_cast<size_t>(B) * NQ * H_q * ns;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    char *p = static_cast<char *>(ws);
+    *ml = reinterpret_cast<float *>(p);
+    p += up(rows * 2 * sizeof(float));
+    *acc = reinterpret_cast<float *>(p);
+    p += up(rows * D * sizeof(float));
+    *cnt = reinterpret_cast<int32_t *>(p);
+}
+
+cudaError_t launch_split(const SplitArgs &a, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+
+// Banded prefill (tcgen05 path).
+struct BandArgs {
+    const void *q, *k, *v;
+    int64_t q_st[3], k_st[3], v_st[3], o_st[3];  // element strides (b, t, h)
+    int B, T, H_q, H_kv, D;
+    int wl, wr;  // < 0: unbounded
+    float scale_log2;
+    const int32_t *global_idx;
+    int n_global;
+    void *o;
+    float *lse;
+    int32_t *counts;
+};
+cudaError_t launch_band(const BandArgs &a, cudaStream_t s);
+unsigned int band_read_clear_error();
+
+}  // namespace swa

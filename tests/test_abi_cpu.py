@@ -1,0 +1,124 @@
+"""The C-ABI library on the host: it loads, exports what include/swa.h declares,
+and rejects invalid arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sliding_window_attention_swa_gb300 as swa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    swa.build()
+    return swa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"SWA_API\s+[\w\s\*]+?\b(swa_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"swa_fwd", "swa_decode", "swa_fwd_workspace_size", "swa_decode_workspace_size",
+            "swa_check_device_error", "swa_status_string", "swa_abi_version"} <= set(names)
+    raw = ctypes.CDLL(swa.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert swa.swa_abi_version() == 1
+    for s in range(6):
+        assert swa.swa_status_string(s)
+    assert "unknown" in swa.swa_status_string(99)
+
+
+def test_struct_sizes_match_header_layout():
+    # fields in declaration order, natural alignment (x86-64 and aarch64 LP64)
+    assert ctypes.sizeof(swa.SwaFwdParams) == 3 * 8 + 9 * 8 + 7 * 4 + 4 + 8 + 4 + 4 + 8 + 24 + 8 + 8
+    assert ctypes.sizeof(swa.SwaDecodeParams) == 5 * 8 + 6 * 4 + 3 * 8
+
+
+def _valid_fwd():
+    p = swa.SwaFwdParams()
+    fake = 0x10000
+    p.q = p.k = p.v = p.o = fake
+    p.lse = fake
+    for name in ("q_strides", "k_strides", "v_strides", "o_strides"):
+        setattr(p, name, (ctypes.c_int64 * 3)(1024 * 64, 64 * 4, 64))
+    p.B, p.T, p.H_q, p.H_kv, p.d_h = 1, 1024, 4, 2, 64
+    p.window_left, p.window_right = 127, 0
+    p.scale = 0.125
+    return p
+
+
+def _valid_decode():
+    p = swa.SwaDecodeParams()
+    fake = 0x10000
+    p.q = p.k_cache = p.v_cache = p.slot_pos = p.q_pos = p.o = p.lse = fake
+    p.B, p.H_q, p.H_kv, p.d_h, p.W = 2, 8, 2, 128, 256
+    p.scale = 0.1
+    return p
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: setattr(p, "q", None), 1),
+    (lambda p: setattr(p, "lse", None), 1),
+    (lambda p: setattr(p, "T", 0), 1),
+    (lambda p: setattr(p, "H_kv", 3), 1),
+    (lambda p: setattr(p, "n_global", 2), 1),          # no global_idx pointer
+    (lambda p: setattr(p, "scale", float("nan")), 1),
+    (lambda p: setattr(p, "d_h", 96), 2),
+    (lambda p: (setattr(p, "H_q", 34), setattr(p, "H_kv", 2)), 2),  # group 17 > 16
+    (lambda p: setattr(p, "scale", -1.0), 2),
+    (lambda p: setattr(p, "q", 0x10008), 2),           # misaligned
+    (lambda p: setattr(p, "k_strides", (ctypes.c_int64 * 3)(100, 10, 3)), 2),
+])
+def test_fwd_rejects(lib, mutate, status):
+    p = _valid_fwd()
+    mutate(p)
+    assert lib.swa_fwd(ctypes.byref(p), None, 0, None) == status
+    assert lib.swa_fwd_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_fwd_workspace_needed_for_globals(lib):
+    p = _valid_fwd()
+    assert lib.swa_fwd_workspace_size(ctypes.byref(p)) == 0
+    p.global_idx = 0x20000
+    p.n_global = 2
+    need = lib.swa_fwd_workspace_size(ctypes.byref(p))
+    assert need > 0
+    assert lib.swa_fwd(ctypes.byref(p), None, 0, None) == 5
+    assert lib.swa_fwd(ctypes.byref(p), ctypes.c_void_p(0x100000), need - 1, None) == 5
+    assert lib.swa_fwd(ctypes.byref(p), ctypes.c_void_p(0x100010), need, None) == 5  # not 256-B aligned
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p: setattr(p, "slot_pos", None), 1),
+    (lambda p: setattr(p, "W", 0), 1),
+    (lambda p: setattr(p, "H_kv", 3), 1),
+    (lambda p: setattr(p, "d_h", 80), 2),
+    (lambda p: setattr(p, "v_cache", 0x10004), 2),
+])
+def test_decode_rejects(lib, mutate, status):
+    p = _valid_decode()
+    mutate(p)
+    assert lib.swa_decode(ctypes.byref(p), None, 0, None) == status
+
+
+def test_decode_workspace(lib):
+    p = _valid_decode()
+    need = lib.swa_decode_workspace_size(ctypes.byref(p))
+    assert need > 0
+    assert lib.swa_decode(ctypes.byref(p), None, 0, None) == 5
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        swa.load_library(str(tmp_path / "nope.so"))
