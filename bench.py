@@ -1,0 +1,478 @@
+"""Benchmark: sliding-window attention on one GB300 (or N replicas).
+
+Headline: band-TFLOP/s of swa_fwd on the Mistral-7B-shape causal prefill
+(B=1, T=16384, H_q=32, H_kv=8, d=128, W=4096, bf16; FLOPs = 4*d per attended
+query-key pair).  The same line carries the ring-buffer decode workload
+(64 sequences, W=4096, H_q=32, H_kv=8, d=128; GB/s of algorithmic bytes), the
+Gemma-3 local-layer and Longformer encoder workloads, the end-to-end number
+through host buffers, the roofline of the dominant kernel, the clocks seen
+during the timed region, and the CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 the script runs under torch.distributed (one process per GPU); every
+rank processes its own copy of the workload (independent units, no data-path
+collective) and the whole-job value is N x work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sliding_window_attention_swa_gb300 import inputs as I  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+KERNELS = {"band": "band_fwd_kernel", "split": "split_attn_kernel", "merge": "merge_kernel"}
+
+
+# ----------------------------------------------------------------------------- work counts
+def prefill_pairs(cfg) -> int:
+    """Attended query-key pairs (all batches and query heads), closed form per row."""
+    T, wl, wr = cfg.T, cfg.window_left, cfg.window_right
+    t = np.arange(T, dtype=np.int64)
+    lo = np.zeros(T, dtype=np.int64) if wl < 0 else np.maximum(0, t - wl)
+    hi = np.full(T, T - 1, dtype=np.int64) if wr < 0 else np.minimum(T - 1, t + wr)
+    cnt = hi - lo + 1
+    if cfg.globals_:
+        G = np.asarray(cfg.globals_)
+        cnt = cnt + ((G[None, :] < lo[:, None]) | (G[None, :] > hi[:, None])).sum(axis=1)
+        cnt[G] = T
+    return int(cnt.sum()) * cfg.B * cfg.Hq
+
+
+def prefill_flops(cfg) -> float:
+    return 4.0 * cfg.d * prefill_pairs(cfg)
+
+
+def prefill_bytes(cfg) -> int:
+    """Algorithmic bytes: Q, K, V read once, O and lse written once."""
+    q = cfg.B * cfg.T * cfg.Hq * cfg.d * 2
+    kv = 2 * cfg.B * cfg.T * cfg.Hkv * cfg.d * 2
+    return q + kv + q + cfg.B * cfg.Hq * cfg.T * 4
+
+
+def decode_bytes(cfg, L: np.ndarray) -> int:
+    """Algorithmic bytes: the valid slots' K and V, all slot positions, q, o, lse."""
+    kv = int(np.minimum(L, cfg.W).sum()) * cfg.Hkv * cfg.d * 2 * 2
+    return kv + cfg.B * cfg.W * 4 + 2 * cfg.B * cfg.Hq * cfg.d * 2 + cfg.B * cfg.Hq * 4 + cfg.B * 4
+
+
+def decode_flops(cfg, L: np.ndarray) -> float:
+    return 4.0 * cfg.d * int(np.minimum(L, cfg.W).sum()) * cfg.Hq
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- device timing
+def to_dev(bits, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def timed_steps(fn, steps: int, warmup: int, flush, stream, sampler=None):
+    """W untimed warm-up calls, then K calls each bracketed by CUDA events on `stream`
+    with an L2 flush (a 256 MB write) before each call, outside its events.  The
+    optional clock sampler runs only around the K timed calls."""
+    import torch
+
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with (sampler or _Null()):
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    return np.array([a.elapsed_time(b) for a, b in ev])  # ms
+
+
+def measure_prefill(cfg, steps, warmup, device, flush, sampler=None):
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    q, k, v = I.prefill_inputs(cfg)
+    qd, kd, vd = to_dev(q, device), to_dev(k, device), to_dev(v, device)
+    del q, k, v
+    g = torch.tensor(cfg.globals_, dtype=torch.int32, device=device) if cfg.globals_ else None
+    o = torch.empty_like(qd)
+    lse = torch.empty((cfg.B, cfg.Hq, cfg.T), dtype=torch.float32, device=device)
+    p = swa.fwd_params(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o, lse, None)
+    need = swa.swa_fwd_workspace_size(p)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        swa.swa_fwd(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o=o, lse=lse, workspace=ws,
+                    stream=stream)
+
+    ms = timed_steps(run, steps, warmup, flush, stream, sampler)
+    swa.swa_check_device_error()
+    launches = 1 + (2 if cfg.globals_ else 0)
+    return {"ms": ms, "flops": prefill_flops(cfg), "bytes": prefill_bytes(cfg), "launches_per_step": launches,
+            "tensors": (qd, kd, vd, g, o, lse, ws)}
+
+
+def measure_decode(cfg, steps, warmup, device, flush):
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    q, kc, vc, pos, qpos = I.decode_inputs(cfg)
+    L = qpos.astype(np.int64) + 1
+    qd, kd, vd = to_dev(q, device), to_dev(kc, device), to_dev(vc, device)
+    del kc, vc
+    posd = torch.from_numpy(pos).to(device)
+    qposd = torch.from_numpy(qpos).to(device)
+    o = torch.empty_like(qd)
+    lse = torch.empty((cfg.B, cfg.Hq), dtype=torch.float32, device=device)
+    p = swa.decode_params(qd, kd, vd, posd, qposd, cfg.scale, o, lse, None)
+    ws = torch.empty(swa.swa_decode_workspace_size(p), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        swa.swa_decode(qd, kd, vd, posd, qposd, cfg.scale, o=o, lse=lse, workspace=ws, stream=stream)
+
+    ms = timed_steps(run, steps, warmup, flush, stream)
+    swa.swa_check_device_error()
+    return {"ms": ms, "flops": decode_flops(cfg, L), "bytes": decode_bytes(cfg, L), "launches_per_step": 2}
+
+
+def measure_e2e_prefill(cfg, steps, warmup, device, dev_tensors):
+    """Same metric through the public call with host buffers: pinned H2D of q/k/v,
+    swa_fwd, D2H of o and lse, every step, all inside the timed region."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    qd, kd, vd, g, o, lse, ws = dev_tensors
+    hq = torch.empty(qd.shape, dtype=qd.dtype, pin_memory=True).copy_(qd)
+    hk = torch.empty(kd.shape, dtype=kd.dtype, pin_memory=True).copy_(kd)
+    hv = torch.empty(vd.shape, dtype=vd.dtype, pin_memory=True).copy_(vd)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        swa.swa_fwd(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o=o, lse=lse, workspace=ws,
+                    stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return ms, h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+class OracleSampler:
+    """Times the fp64 oracle on bounded samples of query rows (uniform over the
+    batch, heads and sequence) of a prefill workload."""
+
+    def __init__(self, cfg, seed: int = 1):
+        import oracle
+
+        self.oracle = oracle
+        self.cfg = cfg
+        self.G = list(cfg.globals_) or None
+        self.q, self.k, self.v = I.prefill_inputs(cfg)
+        self.rng = np.random.default_rng(seed)
+        cal = self.rows(256)
+        t0 = time.perf_counter()
+        self.run(cal)
+        self.sec_per_row = max((time.perf_counter() - t0) / 256, 1e-7)
+
+    def rows(self, n):
+        c = self.cfg
+        return np.stack([self.rng.integers(0, c.B, n), self.rng.integers(0, c.Hq, n),
+                         self.rng.integers(0, c.T, n)], axis=1).astype(np.int64)
+
+    def pairs(self, rows):
+        c, t = self.cfg, rows[:, 2]
+        lo = np.zeros_like(t) if c.window_left < 0 else np.maximum(0, t - c.window_left)
+        hi = np.full_like(t, c.T - 1) if c.window_right < 0 else np.minimum(c.T - 1, t + c.window_right)
+        return int((hi - lo + 1).sum())
+
+    def run(self, rows):
+        c = self.cfg
+        self.oracle.fwd(self.q, self.k, self.v, c.window_left, c.window_right, c.scale, self.G, rows=rows)
+
+    def step(self, budget_s: float):
+        """One timed sample of about budget_s seconds: (TFLOP/s, rows, seconds)."""
+        n = int(max(64, budget_s / self.sec_per_row))
+        rows = self.rows(n)
+        t0 = time.perf_counter()
+        self.run(rows)
+        dt = time.perf_counter() - t0
+        return 4.0 * self.cfg.d * self.pairs(rows) / dt / 1e12, n, dt
+
+    def threads(self) -> int:
+        return self.oracle.num_threads()
+
+
+# ----------------------------------------------------------------------------- main
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    if n_gpus <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = I.MISTRAL
+    sampler = OracleSampler(cfg)
+    budget = min(10.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, n, dt = sampler.step(budget)
+        if i >= args.warmup:
+            vals.append((v, n, dt, sampler.threads()))
+    value = float(np.mean([x[0] for x in vals]))
+    line = {
+        "impl": "reference", "metric": "SWA prefill band-TFLOP/s (fp64 CPU oracle, bounded row sample)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": float(np.mean([x[2] for x in vals]) * 1e3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "H_q": cfg.Hq, "H_kv": cfg.Hkv, "d_h": cfg.d,
+                   "window": cfg.window_left + 1},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0][3], "kind": "oracle",
+                         "sample": f"about {int(np.mean([x[1] for x in vals]))} random query rows of the "
+                                   f"workload per step ({budget:.2f} s of fp64 work)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, help="comma list of workloads: mistral,decode,gemma,longformer")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    swa.load_library()
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer"}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    out = {}
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) if world == 1 else local
+    clocks = None
+    # headline: Mistral-shape prefill
+    barrier()
+    cs = ClockSampler(gpu_index)
+    res = measure_prefill(I.MISTRAL, args.steps, args.warmup, device, flush, cs)
+    barrier()
+    clocks = cs.summary()
+    ms = max_over_ranks(float(res["ms"].mean()))
+    flops = res["flops"]
+    tflops = world * flops / (ms * 1e-3) / 1e12
+    kernel_tflops = flops / (float(res["ms"].mean()) * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = measure_e2e_prefill(I.MISTRAL, max(10, args.steps // 10), args.warmup, device, res["tensors"])
+    e2e_ms = max_over_ranks(e2e_ms)
+    del res["tensors"]
+
+    secondary = {}
+    gpu_launches = res["launches_per_step"] * args.steps
+    if "decode" in only:
+        d = measure_decode(I.DECODE, args.steps, args.warmup, device, flush)
+        dms = max_over_ranks(float(d["ms"].mean()))
+        gbs = world * d["bytes"] / (dms * 1e-3) / 1e9
+        secondary["decode"] = {
+            "workload": I.DECODE.name, "value": gbs, "unit": "GB/s", "ms_per_step": dms,
+            "algorithmic_bytes": d["bytes"], "roofline": {"bound": "hbm", "achieved": d["bytes"] / (float(d["ms"].mean()) * 1e-3) / 1e9,
+                                                          "peak": hbm_peak, "unit": "GB/s",
+                                                          "frac": d["bytes"] / (float(d["ms"].mean()) * 1e-3) / 1e9 / hbm_peak,
+                                                          "peak_kind": peak_kind}}
+        gpu_launches += d["launches_per_step"] * args.steps
+    for key, cfg in (("gemma", I.GEMMA_LOCAL), ("longformer", I.LONGFORMER)):
+        if key not in only:
+            continue
+        r = measure_prefill(cfg, max(20, args.steps // 4), args.warmup, device, flush)
+        del r["tensors"]
+        rms = max_over_ranks(float(r["ms"].mean()))
+        secondary[key] = {
+            "workload": cfg.name, "value": world * r["flops"] / (rms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": rms, "frac_of_bf16_peak": r["flops"] / (rms * 1e-3) / 1e12 / bf16_peak,
+            "hbm_gbs": r["bytes"] / (rms * 1e-3) / 1e9, "frac_of_hbm_peak": r["bytes"] / (rms * 1e-3) / 1e9 / hbm_peak}
+        gpu_launches += r["launches_per_step"] * max(20, args.steps // 4)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        osamp = OracleSampler(I.MISTRAL)
+        v, n, dt = osamp.step(12.0)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": osamp.threads(), "kind": "oracle",
+               "sample": f"{n} random query rows of the Mistral-shape workload ({dt:.1f} s, fp64)"}
+
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "band_fwd_mistral_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                traffic = json.load(f).get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    if rank == 0:
+        line = {
+            "metric": "SWA prefill band-TFLOP/s (Mistral-shape causal prefill); decode GB/s in secondary",
+            "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": I.MISTRAL.name, "B": I.MISTRAL.B, "T": I.MISTRAL.T, "H_q": I.MISTRAL.Hq,
+                       "H_kv": I.MISTRAL.Hkv, "d_h": I.MISTRAL.d, "window": I.MISTRAL.window_left + 1,
+                       "causal": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed (256 MB write) before every timed step",
+                       "flops_per_step": flops},
+            "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": kernel_tflops / bf16_peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)", "kernel": KERNELS["band"]},
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
