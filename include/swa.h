@@ -157,6 +157,12 @@ SWA_API swa_status swa_decode(const swa_decode_params *p, void *workspace, size_
  */
 SWA_API swa_status swa_check_device_error(swa_stream_t stream);
 
+/*
+ * Description of the CUDA error behind the most recent SWA_ERR_CUDA returned to the
+ * calling host thread ("no error" if none).  The string is static.
+ */
+SWA_API const char *swa_last_error_string(void);
+
 /* Static description of a status code. */
 SWA_API const char *swa_status_string(swa_status s);
 

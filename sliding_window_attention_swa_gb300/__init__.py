@@ -57,7 +57,10 @@ STATUS = {0: "SWA_OK", 1: "SWA_ERR_INVALID_ARG", 2: "SWA_ERR_UNSUPPORTED", 3: "S
 class SwaError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} returned {STATUS.get(status, status)}: {swa_status_string(status)}")
+        msg = f"{fn} returned {STATUS.get(status, status)}: {swa_status_string(status)}"
+        if status == 3:
+            msg += f" ({load_library().swa_last_error_string().decode()})"
+        super().__init__(msg)
 
 
 _lib = None
@@ -92,6 +95,8 @@ def load_library(path: str | None = None):
     lib.swa_decode.restype = ctypes.c_int
     lib.swa_check_device_error.argtypes = [vp]
     lib.swa_check_device_error.restype = ctypes.c_int
+    lib.swa_last_error_string.argtypes = []
+    lib.swa_last_error_string.restype = ctypes.c_char_p
     lib.swa_status_string.argtypes = [ctypes.c_int]
     lib.swa_status_string.restype = ctypes.c_char_p
     lib.swa_abi_version.argtypes = []

@@ -17,6 +17,15 @@ bool strides_ok(const int64_t st[3]) {
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 constexpr float kLog2e = 1.4426950408889634f;
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Records a failed CUDA call for swa_last_error_string(); true if `e` is a failure.
+bool failed(cudaError_t e) {
+    if (e == cudaSuccess) return false;
+    t_last_cuda_error = e;
+    return true;
+}
+
 swa_status fwd_check(const swa_fwd_params *p) {
     if (!p || !p->q || !p->k || !p->v || !p->o || !p->lse) return SWA_ERR_INVALID_ARG;
     if (p->B < 1 || p->T < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1) return SWA_ERR_INVALID_ARG;
@@ -64,6 +73,8 @@ swa_status workspace_ok(void *ws, size_t have, size_t need) {
 extern "C" {
 
 int32_t swa_abi_version(void) { return SWA_ABI_VERSION; }
+
+const char *swa_last_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char *swa_status_string(swa_status s) {
     switch (s) {
@@ -113,7 +124,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
     ba.n_global = p->n_global;
     ba.lse = p->lse;
     ba.counts = p->row_counts;
-    if (swa::launch_band(ba, s) != cudaSuccess) return SWA_ERR_CUDA;
+    if (failed(swa::launch_band(ba, s))) return SWA_ERR_CUDA;
 
     if (p->n_global > 0) {
         // Global rows attend to all T keys: split-K over T, merged by log-sum-exp,
@@ -148,7 +159,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
         swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T, &sa.ws_ml, &sa.ws_acc,
                          &sa.ws_cnt);
-        if (swa::launch_split(sa, s) != cudaSuccess) return SWA_ERR_CUDA;
+        if (failed(swa::launch_split(sa, s))) return SWA_ERR_CUDA;
         swa::MergeArgs ma{};
         ma.ws_ml = sa.ws_ml;
         ma.ws_acc = sa.ws_acc;
@@ -173,7 +184,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         ma.cnt_sb = ma.lse_sb;
         ma.cnt_sh = ma.lse_sh;
         ma.cnt_st = 1;
-        if (swa::launch_merge(ma, s) != cudaSuccess) return SWA_ERR_CUDA;
+        if (failed(swa::launch_merge(ma, s))) return SWA_ERR_CUDA;
     }
     return SWA_OK;
 }
@@ -217,7 +228,7 @@ swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t worksp
     sa.n_splits = swa::split_count(p->W);
     sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
     swa::split_carve(workspace, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
-    if (swa::launch_split(sa, s) != cudaSuccess) return SWA_ERR_CUDA;
+    if (failed(swa::launch_split(sa, s))) return SWA_ERR_CUDA;
 
     swa::MergeArgs ma{};
     ma.ws_ml = sa.ws_ml;
@@ -243,12 +254,12 @@ swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t worksp
     ma.cnt_sb = p->H_q;
     ma.cnt_sh = 1;
     ma.cnt_st = 0;
-    if (swa::launch_merge(ma, s) != cudaSuccess) return SWA_ERR_CUDA;
+    if (failed(swa::launch_merge(ma, s))) return SWA_ERR_CUDA;
     return SWA_OK;
 }
 
 swa_status swa_check_device_error(swa_stream_t stream) {
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SWA_ERR_CUDA;
+    if (failed(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)))) return SWA_ERR_CUDA;
     const unsigned int e = swa::band_read_clear_error();
     return e ? SWA_ERR_TIMEOUT : SWA_OK;
 }

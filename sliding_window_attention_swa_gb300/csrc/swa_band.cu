@@ -1,36 +1,36 @@
 // swa_band.cu -- banded (sliding-window) attention prefill on 5th-generation
 // tensor cores (sm_103a).
 //
-// Work unit: one (batch b, key/value head kvh, query tile).  A query tile is 128
-// rows = TQ consecutive tokens x the G = H_q/H_kv query heads of the group
-// (row = token_local * G + head_local), so every key/value tile is loaded once
-// for the whole group.  The unit iterates only over the key tiles that intersect
-// the union of its rows' bands
+// Work unit: one (batch b, key/value head kvh, group of NQT query tiles).  A query
+// tile is 128 rows = TQ consecutive tokens x the G = H_q/H_kv query heads of the
+// group (row = token_local * G + head_local), so every key/value tile is loaded
+// once for the whole group.  The unit iterates only over the key tiles that
+// intersect the union of its rows' bands
 //     [max(0, t_first - wl), min(T-1, t_last + wr)]
-// (keys outside the window are never loaded or scored; the production
-// kernels described in "Sliding Window Attention", lizeman.github.io
-// llm-arch-kb section 3, and in the superteams.ai glossary, iterate over the
-// band only), followed by ceil(n_global / BN) "global column" tiles that hold the
-// key/value rows of the global positions (prathamp.com "Sliding Window
-// Attention: From Local Windows to Global Context", section 4.3).
+// -- keys outside the window are never loaded or scored, as in the production
+// kernels described by "Sliding Window Attention" (lizeman.github.io llm-arch-kb,
+// section 3) and the superteams.ai glossary -- followed by ceil(n_global / BN)
+// "global column" tiles holding the key/value rows of the global positions
+// (prathamp.com "Sliding Window Attention: From Local Windows to Global Context",
+// section 4.3).
 //
-// Roles (192 threads):
-//   warp 0      TMA producer: Q once; K and V tiles into a STAGES-deep ring;
-//               global-column tiles are gathered with plain loads into the same
-//               swizzled layout.
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S[j&1] = Q K_j^T          (tcgen05.mma, M=128, N=BN, K=D)
-//                 O     += P_{j-1} V_{j-1}  (tcgen05.mma, M=128, N=D, K=BN)
-//               S is double-buffered in TMEM so S_{j+1} runs while the softmax
-//               works on S_j.
-//   warps 2..5  softmax (one TMEM lane = one row per thread): mask (edge tiles
-//               and global tiles only), running max in the log2 domain, P =
-//               2^(x - m) written as bf16 to shared memory (K-major, 128B
-//               swizzle) for the PV MMA, running sum l.  The O accumulator in
-//               TMEM is rescaled only when a row's max grows by more than 2^8
-//               (the result is exact either way: numerator and denominator share
-//               the stale max).  Epilogue: O / l -> bf16 -> TMA store; lse and
-//               attended-key counts per row.
+// Roles:
+//   warp 0        producer: Q tiles once (TMA); then K_0, V_0, K_1, V_1, ... into
+//                 a ring of NSLOT shared-memory slots (TMA for band tiles, plain
+//                 gathers into the same 128B-swizzled layout for global tiles).
+//   warp 1        TMEM owner and MMA issuer (one thread):
+//                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
+//                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
+//   warps 2..     NQT softmax warpgroups; one row per thread (TMEM lane).  Scores
+//                 are masked only on band-edge and global tiles; the running max is
+//                 kept in the log2 domain; P = 2^(x - m) is written back as bf16 over
+//                 the S columns it came from; O is rescaled in TMEM only when a row's
+//                 max grows by more than 2^8 (numerator and denominator share the
+//                 stale max, so the result is exact either way).  Epilogue: O / l ->
+//                 bf16 -> TMA store; lse and attended-key counts per row.
+// NQT = 2 (head dim <= 128): two query tiles ping-pong -- while one warpgroup turns
+// S_A into P_A the tensor cores run S_B and P_B V -- with TMEM S_A | S_B | O_A | O_B.
+// NQT = 1 (head dim 256): one query tile, S double-buffered, TMEM S0 | S1 | O.
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and MMAs, frees TMEM and returns.
 #include <cfloat>
@@ -46,41 +46,49 @@ namespace {
 
 __device__ unsigned int g_band_err = 0;
 
-constexpr int BM = 128;          // query rows per unit (TMEM lanes)
-constexpr int kThreads = 192;    // 6 warps
+constexpr int BM = 128;              // query rows per tile (TMEM lanes)
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 template <int D>
 struct BandCfg {
-    static constexpr int BN = D == 256 ? 64 : 128;          // keys per tile
-    static constexpr int STAGES = D == 64 ? 4 : 2;           // K/V ring depth
-    static constexpr int QBYTES = BM * D * 2;
-    static constexpr int KVBYTES = BN * D * 2;               // one K (or V) tile
-    static constexpr int PBYTES = BM * BN * 2;               // one P buffer
+    static constexpr int NQT = D <= 128 ? 2 : 1;     // query tiles per CTA
+    static constexpr int BN = D == 256 ? 64 : 128;  // keys per K/V tile
+    // NQT = 2: warpgroup 0 = producer warp, MMA warp, two idle warps; warpgroups 1, 2 =
+    // softmax.  Twelve warps put three on each SM sub-partition, whose 16K-register
+    // file caps the launch at 168 registers a thread; setmaxnreg then moves registers
+    // from warpgroup 0 (56) to the softmax warpgroups (224):
+    //   128 * 56 + 256 * 224 = 64512 = 384 * 168.
+    // NQT = 1: producer warp, MMA warp and one softmax warpgroup (192 threads).
+    static constexpr int THREADS = NQT == 2 ? 384 : 192;
+    static constexpr int SOFTMAX_WARP0 = NQT == 2 ? 4 : 2;
+    static constexpr int REG_LAUNCH = NQT == 2 ? 168 : 255;
+    static constexpr int REG_CTRL = 56, REG_SOFTMAX = 224;
+    static_assert(NQT == 1 || 128 * REG_CTRL + 256 * REG_SOFTMAX <= THREADS * REG_LAUNCH, "register split");
+    static constexpr int QBYTES = BM * D * 2;        // one query tile (reused for O staging)
+    static constexpr int TBYTES = BN * D * 2;        // one K or V tile
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + QBYTES;
-    static constexpr int OFF_V = OFF_K + STAGES * KVBYTES;
-    static constexpr int OFF_P = OFF_V + STAGES * KVBYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * PBYTES;
-    // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], s_empty[2], p_full[2],
-    // pv_done[2], drain
-    static constexpr int NBAR = 1 + 3 * STAGES + 8 + 1;
+    static constexpr int OFF_RING = NQT * QBYTES;
+    static constexpr int NSLOT = (232448 - 2048 - OFF_RING) / TBYTES;
+    static constexpr int OFF_BAR = OFF_RING + NSLOT * TBYTES;
+    // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_done[2], pv_done[2], drain
+    static constexpr int NBAR = 1 + 2 * NSLOT + 9;
     static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;      // + slack for 1024-B alignment
+    static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;  // + slack for 1024-B alignment
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_O = 0;                       // O accumulator columns [0, D)
-    static constexpr uint32_t TM_S = 256;                     // S buffers at 256 and 256 + BN
+    __host__ __device__ static constexpr uint32_t tm_s(int slot) { return static_cast<uint32_t>(slot * BN); }
+    __host__ __device__ static constexpr uint32_t tm_o(int tile) { return 256u + static_cast<uint32_t>(tile * 128); }
+    static_assert(NSLOT >= 3, "K/V ring too shallow");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(D <= 256 && TM_S + 2 * BN <= TMEM_COLS, "tensor memory budget");
+    static_assert(tm_o(NQT - 1) + D <= TMEM_COLS && tm_s(1) + BN <= 256, "tensor memory budget");
 };
 
 struct BandKernelArgs {
-    int B, T, H_q, H_kv, G, TQ, n_qtiles;
+    int B, T, H_q, H_kv, G, TQ, n_units_t;
     int wl, wr;
     float scale_log2;
     const int32_t *global_idx;
     int n_global;
-    const __nv_bfloat16 *k, *v;     // for the global-column gather
+    const __nv_bfloat16 *k, *v;  // for the global-column gather
     int64_t k_st[3], v_st[3];
     float *lse;
     int32_t *counts;
@@ -98,12 +106,12 @@ __device__ __forceinline__ bool in_band(int t, int s, int wl, int wr) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     band_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const BandKernelArgs a) {
     using C = BandCfg<D>;
-    constexpr int BN = C::BN, STAGES = C::STAGES;
+    constexpr int BN = C::BN, NSLOT = C::NSLOT, NQT = C::NQT;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
 
@@ -112,25 +120,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = (sraw + 1023u) & ~1023u;
     uint8_t *sgen = smem_raw + (sbase - sraw);
 
-    const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P;
+    const uint32_t sQ = sbase + C::OFF_Q, sRing = sbase + C::OFF_RING;
     const uint32_t bars = sbase + C::OFF_BAR;
     auto bar_q = [&]() { return bars; };
-    auto bar_kf = [&](int s) { return bars + 8u * (1 + s); };
-    auto bar_vf = [&](int s) { return bars + 8u * (1 + STAGES + s); };
-    auto bar_ke = [&](int s) { return bars + 8u * (1 + 2 * STAGES + s); };
-    auto bar_sf = [&](int b) { return bars + 8u * (1 + 3 * STAGES + b); };
-    auto bar_se = [&](int b) { return bars + 8u * (3 + 3 * STAGES + b); };
-    auto bar_pf = [&](int b) { return bars + 8u * (5 + 3 * STAGES + b); };
-    auto bar_pv = [&](int b) { return bars + 8u * (7 + 3 * STAGES + b); };
-    const uint32_t bar_drain = bars + 8u * (9 + 3 * STAGES);
+    auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto bar_empty = [&](int s) { return bars + 8u * (1 + NSLOT + s); };
+    auto bar_sf = [&](int i) { return bars + 8u * (1 + 2 * NSLOT + i); };
+    auto bar_pf = [&](int i) { return bars + 8u * (3 + 2 * NSLOT + i); };
+    auto bar_od = [&](int i) { return bars + 8u * (5 + 2 * NSLOT + i); };
+    auto bar_pv = [&](int i) { return bars + 8u * (7 + 2 * NSLOT + i); };
+    const uint32_t bar_drain = bars + 8u * (9 + 2 * NSLOT);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
 
-    // ---- unit decode (longest units first: query tiles in decreasing order)
+    // ---- unit decode (longest units first: query-tile groups in decreasing order)
     const int bh = blockIdx.x % (a.B * a.H_kv);
-    const int qt = a.n_qtiles - 1 - blockIdx.x / (a.B * a.H_kv);
+    const int ut = a.n_units_t - 1 - blockIdx.x / (a.B * a.H_kv);
     const int b = bh / a.H_kv, kvh = bh % a.H_kv;
-    const int t0 = qt * a.TQ;
-    const int t1 = min(a.T - 1, t0 + a.TQ - 1);
+    const int t0 = ut * NQT * a.TQ;
+    const int t1 = min(a.T - 1, t0 + NQT * a.TQ - 1);
     const int kv_lo = a.wl < 0 ? 0 : max(0, t0 - a.wl);
     const int kv_hi = a.wr < 0 ? a.T - 1 : min(a.T - 1, t1 + a.wr);
     const int n_band = (kv_hi - kv_lo + BN) / BN;
@@ -141,15 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(bar_q(), 1);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_kf(s), 1);
-            mbar_init(bar_vf(s), 1);
-            mbar_init(bar_ke(s), 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sf(i), 1);
-            mbar_init(bar_se(i), 4);
             mbar_init(bar_pf(i), 4);
+            mbar_init(bar_od(i), 1);
             mbar_init(bar_pv(i), 1);
         }
         mbar_init(bar_drain, 1);
@@ -173,35 +179,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ============================ producer ============================
-        int last_tile[STAGES];
-#pragma unroll
-        for (int s = 0; s < STAGES; ++s) last_tile[s] = -1;
-        bool ok = true;
+        if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
+        int n_issued = 0;  // ring fills issued so far
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_q(), static_cast<uint32_t>(a.G * a.TQ * D * 2));
+            uint32_t qbytes = 0;
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d(sQ + c * (BM * 128), &tm_q, bar_q(), c * 64, kvh * a.G, t0, b);
+            for (int x = 0; x < NQT; ++x)
+                if (t0 + x * a.TQ < a.T) qbytes += static_cast<uint32_t>(a.G * a.TQ * D * 2);
+            mbar_arrive_expect_tx(bar_q(), qbytes);
+#pragma unroll
+            for (int x = 0; x < NQT; ++x) {
+                if (t0 + x * a.TQ >= a.T) continue;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(sQ + x * C::QBYTES + c * (BM * 128), &tm_q, bar_q(), c * 64, kvh * a.G,
+                                t0 + x * a.TQ, b);
+            }
         }
+        bool ok = true;
 #pragma unroll 1
-        for (int j = 0; j < n_tiles && ok; ++j) {
-            const int s = j % STAGES;
-            if (j >= STAGES) ok = warp_wait(bar_ke(s), ((j / STAGES) - 1) & 1, abort);
+        for (int i = 0; i < 2 * n_tiles; ++i) {
+            const int s = i % NSLOT;
+            if (i >= NSLOT) ok = warp_wait(bar_empty(s), ((i / NSLOT) - 1) & 1, abort);
             if (!ok) break;
-            const uint32_t kd = sK + s * C::KVBYTES, vd = sV + s * C::KVBYTES;
+            const int j = i >> 1;
+            const bool is_v = (i & 1) != 0;
+            const uint32_t dst = sRing + s * C::TBYTES;
             if (j < n_band) {
                 if (lane == 0) {
                     const int k0 = kv_lo + j * BN;
-                    mbar_arrive_expect_tx(bar_kf(s), C::KVBYTES);
+                    mbar_arrive_expect_tx(bar_full(s), C::TBYTES);
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) tma_load_4d(kd + c * (BN * 128), &tm_k, bar_kf(s), c * 64, kvh, k0, b);
-                    mbar_arrive_expect_tx(bar_vf(s), C::KVBYTES);
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c) tma_load_4d(vd + c * (BN * 128), &tm_v, bar_vf(s), c * 64, kvh, k0, b);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d(dst + c * (BN * 128), is_v ? &tm_v : &tm_k, bar_full(s), c * 64, kvh, k0, b);
                 }
             } else {
-                // global-column tile: gather rows global_idx[jg*BN + r] (zero rows past the list)
+                // global-column tile: rows global_idx[g0 + r] (zero rows past the list)
                 const int g0 = (j - n_band) * BN;
+                const __nv_bfloat16 *src = is_v ? a.v : a.k;
+                const int64_t *st = is_v ? a.v_st : a.k_st;
                 constexpr int kPieces = D / 8;
                 for (int idx = lane; idx < BN * kPieces; idx += 32) {
                     const int r = idx / kPieces, pc = idx % kPieces;
@@ -211,119 +227,167 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int gs = a.global_idx[gi];
                         if (gs >= 0 && gs < a.T) srow = gs;
                     }
-                    uint4 kx = make_uint4(0, 0, 0, 0), vx = make_uint4(0, 0, 0, 0);
-                    if (srow >= 0) {
-                        const int64_t eb = static_cast<int64_t>(b);
-                        kx = *reinterpret_cast<const uint4 *>(a.k + eb * a.k_st[0] + static_cast<int64_t>(srow) * a.k_st[1] +
-                                                              static_cast<int64_t>(kvh) * a.k_st[2] + pc * 8);
-                        vx = *reinterpret_cast<const uint4 *>(a.v + eb * a.v_st[0] + static_cast<int64_t>(srow) * a.v_st[1] +
-                                                              static_cast<int64_t>(kvh) * a.v_st[2] + pc * 8);
-                    }
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (srow >= 0)
+                        val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(b) * st[0] +
+                                                               static_cast<int64_t>(srow) * st[1] +
+                                                               static_cast<int64_t>(kvh) * st[2] + pc * 8);
                     const uint32_t off = (pc >> 3) * (BN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sgen + C::OFF_K + s * C::KVBYTES + off) = kx;
-                    *reinterpret_cast<uint4 *>(sgen + C::OFF_V + s * C::KVBYTES + off) = vx;
+                    *reinterpret_cast<uint4 *>(sgen + C::OFF_RING + s * C::TBYTES + off) = val;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_kf(s));
-                    mbar_arrive(bar_vf(s));
-                }
+                if (lane == 0) mbar_arrive(bar_full(s));
             }
-            last_tile[s] = j;
+            n_issued = i + 1;
         }
         if (!ok && lane == 0) {
-            // drain the copies still in flight before the CTA exits
+            // drain the copies still in flight (at most the last NSLOT fills) before exit
             mbar_drain(bar_q(), 0, &g_band_err);
-#pragma unroll
-            for (int s = 0; s < STAGES; ++s)
-                if (last_tile[s] >= 0 && last_tile[s] < n_band) {
-                    mbar_drain(bar_kf(s), (last_tile[s] / STAGES) & 1, &g_band_err);
-                    mbar_drain(bar_vf(s), (last_tile[s] / STAGES) & 1, &g_band_err);
-                }
+            for (int i = max(0, n_issued - NSLOT); i < n_issued; ++i)
+                if ((i >> 1) < n_band) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
+        if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait(bar_q(), 0, abort, &g_band_err);
-            auto issue_pv = [&](int i) -> bool {
-                const int s = i % STAGES, pb = i & 1;
-                if (!mbar_wait(bar_pf(pb), (i >> 1) & 1, abort, &g_band_err)) return false;
-                if (!mbar_wait(bar_vf(s), (i / STAGES) & 1, abort, &g_band_err)) return false;
+            // S into TMEM slot `slot` from query tile `qt` and the K tile of key tile j.
+            auto mma_s = [&](int slot, int qt, int j, bool wait_k) -> bool {
+                const int fi = 2 * j, s = fi % NSLOT;
+                if (wait_k && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
-                const uint32_t pbase = sP + pb * C::PBYTES, vbase = sV + s * C::KVBYTES;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = smem_desc(pbase + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(vbase + kk * 2048, BN * 128, 1024, kSwizzle128B);
-                    tc_mma_ss(tmem + C::TM_O, ad, bd, idPV, (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(bar_pv(pb));
-                tc_commit(bar_ke(s));
-                return true;
-            };
-#pragma unroll 1
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j % STAGES, sb = j & 1;
-                ok = mbar_wait(bar_kf(s), (j / STAGES) & 1, abort, &g_band_err);
-                if (ok && j >= 2) ok = mbar_wait(bar_se(sb), ((j >> 1) - 1) & 1, abort, &g_band_err);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kbase = sK + s * C::KVBYTES;
+                const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = smem_desc(sQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(kbase + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    tc_mma_ss(tmem + C::TM_S + sb * BN, ad, bd, idS, kk > 0 ? 1u : 0u);
+                    const uint64_t ad = smem_desc(qb + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bd = smem_desc(kb + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    tc_mma_ss(tmem + C::tm_s(slot), ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar_sf(sb));
-                if (j >= 1) ok = issue_pv(j - 1);
+                return true;
+            };
+            // O_tile += P(slot) V_j
+            auto mma_pv = [&](int slot, int otile, int j, int p_parity, bool wait_v) -> bool {
+                const int fi = 2 * j + 1, s = fi % NSLOT;
+                if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
+                if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
+                tc_fence_after();
+                const uint32_t vb = sRing + s * C::TBYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bd = smem_desc(vb + kk * 2048, BN * 128, 1024, kSwizzle128B);
+                    tc_mma_ts(tmem + C::tm_o(otile), tmem + C::tm_s(slot) + kk * 8, bd, idPV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                return true;
+            };
+            auto kslot = [&](int j) { return (2 * j) % NSLOT; };
+            auto vslot = [&](int j) { return (2 * j + 1) % NSLOT; };
+            if constexpr (NQT == 2) {
+                if (ok) ok = mma_s(0, 0, 0, true);
+                if (ok) {
+                    tc_commit(bar_sf(0));
+                    ok = mma_s(1, 1, 0, false);
+                }
+                if (ok) {
+                    tc_commit(bar_sf(1));
+                    tc_commit(bar_empty(kslot(0)));
+                }
+#pragma unroll 1
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    ok = mma_pv(0, 0, j, j & 1, true);
+                    if (!ok) break;
+                    if (j + 1 < n_tiles) {
+                        ok = mma_s(0, 0, j + 1, true);
+                        if (!ok) break;
+                        tc_commit(bar_sf(0));
+                    } else {
+                        tc_commit(bar_od(0));
+                    }
+                    ok = mma_pv(1, 1, j, j & 1, false);
+                    if (!ok) break;
+                    tc_commit(bar_empty(vslot(j)));
+                    if (j + 1 < n_tiles) {
+                        ok = mma_s(1, 1, j + 1, false);
+                        if (!ok) break;
+                        tc_commit(bar_sf(1));
+                        tc_commit(bar_empty(kslot(j + 1)));
+                    } else {
+                        tc_commit(bar_od(1));
+                    }
+                }
+            } else {
+                if (ok) ok = mma_s(0, 0, 0, true);
+                if (ok) {
+                    tc_commit(bar_sf(0));
+                    tc_commit(bar_empty(kslot(0)));
+                }
+#pragma unroll 1
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    if (j + 1 < n_tiles) {
+                        // slot (j+1)&1 last held P_{j-1}, consumed by PV_{j-1} issued earlier
+                        ok = mma_s((j + 1) & 1, 0, j + 1, true);
+                        if (!ok) break;
+                        tc_commit(bar_sf((j + 1) & 1));
+                        tc_commit(bar_empty(kslot(j + 1)));
+                    }
+                    ok = mma_pv(j & 1, 0, j, (j >> 1) & 1, true);
+                    if (!ok) break;
+                    tc_commit(bar_pv(j & 1));
+                    tc_commit(bar_empty(vslot(j)));
+                    if (j + 1 == n_tiles) tc_commit(bar_od(0));
+                }
             }
-            if (ok && n_tiles > 0) ok = issue_pv(n_tiles - 1);
             if (!ok) {
                 tc_commit(bar_drain);
                 mbar_drain(bar_drain, 0, &g_band_err);
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= C::SOFTMAX_WARP0) {
         // ============================ softmax / epilogue ============================
+        if constexpr (NQT == 2) regs_inc<C::REG_SOFTMAX>();
+        const int wg = (warp - C::SOFTMAX_WARP0) >> 2;  // query tile of this warpgroup
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;             // row == TMEM lane
+        const int r = quarter * 32 + lane;  // row == TMEM lane
+        const int tx = t0 + wg * a.TQ;      // first token of this warpgroup's query tile
         const int tq = r / a.G, hj = r % a.G;
-        const int t = t0 + tq;
+        const int t = tx + tq;
         const bool row_ok = tq < a.TQ && t < a.T;
         const int h = kvh * a.G + hj;
+        const int tlo = tx, thi = min(a.T - 1, tx + a.TQ - 1);
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t o_addr = tmem + lane_addr + C::tm_o(wg);
         float m = -INFINITY, l = 0.f;
         int count = 0;
         bool ok = true;
 #pragma unroll 1
         for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            if (!warp_wait(bar_sf(sb), (j >> 1) & 1, abort)) { ok = false; break; }
+            const int slot = NQT == 2 ? wg : (j & 1);
+            const uint32_t parity = NQT == 2 ? (j & 1) : ((j >> 1) & 1);
+            if (!warp_wait(bar_sf(slot), parity, abort)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
+            const uint32_t s_addr = tmem + lane_addr + C::tm_s(slot);
             float x[BN];
             {
-                uint32_t raw[32];
+                uint32_t raw[BN / 32][32];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(tmem + lane_addr + C::TM_S + sb * BN + c * 32, raw);
-                    tc_wait_ld();
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, raw[c]);
+                tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[e]);
-                }
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_se(sb));
-
-            // mask
+            // ---- mask
             if (j < n_band) {
                 const int k0 = kv_lo + j * BN;
-                const bool interior = (a.wl < 0 || k0 >= t1 - a.wl) && (a.wr < 0 || k0 + BN - 1 <= t0 + a.wr) &&
+                const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
                                       (k0 + BN - 1 <= a.T - 1);
                 if (interior) {
                     count += BN;
@@ -350,71 +414,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x[c] = al ? x[c] : -INFINITY;
                 }
             }
-            // running max (log2 domain) with lazy rescale
-            float mx = -INFINITY;
+            // ---- running max (log2 domain), tree reduction
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, x[c]);
+            for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < BN; c += 8)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[c + i]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float mt = mx * a.scale_log2;
             const bool need = mt > m + kRescaleTau;
             const float mu = need ? mt : m;
             const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
             if (__any_sync(0xffffffffu, need) && j > 0) {
-                // O holds PV_0 .. PV_{j-1}; wait for the last one, then rescale this warp's rows.
-                if (!warp_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1, abort)) { ok = false; break; }
-                tc_fence_after();
+                // O holds P V of tiles 0 .. j-1 and must be complete before it is rescaled.
+                if constexpr (NQT == 1) {
+                    if (!warp_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
-                    tmem_ld32(tmem + lane_addr + C::TM_O + c * 32, ov);
+                    tmem_ld32(o_addr + c * 32, ov);
                     tc_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(tmem + lane_addr + C::TM_O + c * 32, ov);
+                    tmem_st32(o_addr + c * 32, ov);
                 }
-                tc_wait_st();
             }
             m = mu;
             const float msub = mu == -INFINITY ? 0.f : mu;
-            float rs = 0.f;
-            // P buffer sb was last read by PV_{j-2}
-            if (j >= 2) {
-                if (!warp_wait(bar_pv(sb), ((j - 2) >> 1) & 1, abort)) { ok = false; break; }
-            }
-            uint8_t *pdst = sgen + C::OFF_P + sb * C::PBYTES;
+            // ---- P = 2^(x*scale_log2 - m) as bf16 pairs over the first BN/2 S columns
+            float rs8[8];
 #pragma unroll
-            for (int c8 = 0; c8 < BN / 8; ++c8) {
-                uint32_t w[4];
+            for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2(fmaf(x[c8 * 8 + 2 * e], a.scale_log2, -msub));
-                    const float p1 = ex2(fmaf(x[c8 * 8 + 2 * e + 1], a.scale_log2, -msub));
-                    rs += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
+            for (int hlf = 0; hlf < BN / 64; ++hlf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2(fmaf(x[hlf * 64 + 2 * e], a.scale_log2, -msub));
+                    const float p1 = ex2(fmaf(x[hlf * 64 + 2 * e + 1], a.scale_log2, -msub));
+                    rs8[e & 7] += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
                 }
-                const uint32_t off = (c8 >> 3) * (BM * 128) + r * 128 + (((c8 & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(pdst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                tmem_st32(s_addr + hlf * 32, pk);
             }
-            l = l * alpha + rs;
-            fence_proxy_async_smem();
+            tc_wait_st();
+            l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pf(sb));
+            if (lane == 0) mbar_arrive(bar_pf(slot));
         }
 
         // ---- epilogue
-        if (ok && n_tiles > 0) {
-            ok = warp_wait(bar_pv((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort);
-        }
-        // all four softmax warps agree before touching the Q region (reused as O staging)
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const bool all_ok = *abort == 0 && ok;
+        if (ok) ok = warp_wait(bar_od(wg), 0, abort);
+        const bool all_ok = ok && *abort == 0;
+        const uint32_t stage = sQ + wg * C::QBYTES;  // this tile's Q region, free once O is final
         if (all_ok) {
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
-                tmem_ld32(tmem + lane_addr + C::TM_O + c * 32, ov);
+                tmem_ld32(o_addr + c * 32, ov);
                 tc_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -425,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            __uint_as_float(ov[q4 * 8 + 2 * e + 1]) * inv_l);
                     const int pc = c * 4 + q4;  // 16-byte piece index along d
                     const uint32_t off = (pc >> 3) * (BM * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sgen + C::OFF_Q + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(sgen + C::OFF_Q + wg * C::QBYTES + off) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -435,13 +503,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (a.counts) a.counts[li] = count;
             }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (all_ok && warp == 2 && lane == 0) {
+        // the warpgroup's rows are staged before one of its threads issues the store
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
+        if (all_ok && ((warp - C::SOFTMAX_WARP0) & 3) == 0 && lane == 0 && tx < a.T) {
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) tma_store_4d(&tm_o, sQ + c * (BM * 128), c * 64, kvh * a.G, t0, b);
+            for (int c = 0; c < D / 64; ++c) tma_store_4d(&tm_o, stage + c * (BM * 128), c * 64, kvh * a.G, tx, b);
             tma_store_commit();
             tma_store_wait_all();
         }
+    } else {
+        // idle warps of warpgroup 0 give their registers to the softmax warpgroups
+        if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
     }
 
     tc_fence_before();
@@ -507,7 +579,8 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.H_kv = x.H_kv;
     a.G = G;
     a.TQ = TQ;
-    a.n_qtiles = (x.T + TQ - 1) / TQ;
+    const int n_qtiles = (x.T + TQ - 1) / TQ;
+    a.n_units_t = (n_qtiles + C::NQT - 1) / C::NQT;
     a.wl = x.wl;
     a.wr = x.wr;
     a.scale_log2 = x.scale_log2;
@@ -521,9 +594,9 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     }
     a.lse = x.lse;
     a.counts = x.counts;
-    const long long units = static_cast<long long>(x.B) * x.H_kv * a.n_qtiles;
+    const long long units = static_cast<long long>(x.B) * x.H_kv * a.n_units_t;
     if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    band_fwd_kernel<D><<<static_cast<unsigned>(units), kThreads, C::SMEM, s>>>(mq, mk, mv, mo, a);
+    band_fwd_kernel<D><<<static_cast<unsigned>(units), C::THREADS, C::SMEM, s>>>(mq, mk, mv, mo, a);
     return cudaGetLastError();
 }
 
