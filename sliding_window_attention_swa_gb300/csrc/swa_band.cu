@@ -101,10 +101,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ bool in_band(int t, int s, int wl, int wr) {
-    return (wl < 0 || s >= t - wl) && (wr < 0 || s <= t + wr);
-}
-
 template <int D>
 __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     band_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -358,6 +354,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         const bool row_ok = tq < a.TQ && t < a.T;
         const int h = kvh * a.G + hj;
         const int tlo = tx, thi = min(a.T - 1, tx + a.TQ - 1);
+        // this row's band, clipped to [0, T)
+        const int lo_abs = a.wl < 0 ? 0 : max(0, t - a.wl);
+        const int hi_abs = a.wr < 0 ? a.T - 1 : min(a.T - 1, t + a.wr);
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t o_addr = tmem + lane_addr + C::tm_o(wg);
         float m = -INFINITY, l = 0.f;
@@ -384,7 +383,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
             }
-            // ---- mask
+            // ---- mask (branch-free; only band-edge and global tiles)
             if (j < n_band) {
                 const int k0 = kv_lo + j * BN;
                 const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
@@ -392,27 +391,34 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (interior) {
                     count += BN;
                 } else {
+                    // allowed columns of this row form one run [lo, lo + len)
+                    const int lo = min(max(lo_abs - k0, 0), BN);
+                    const int hi = min(max(hi_abs - k0 + 1, 0), BN);
+                    const int len = max(hi - lo, 0);
+                    count += len;
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        const int sk = k0 + c;
-                        const bool al = sk <= a.T - 1 && in_band(t, sk, a.wl, a.wr);
-                        count += al ? 1 : 0;
-                        x[c] = al ? x[c] : -INFINITY;
-                    }
+                    for (int c = 0; c < BN; ++c)
+                        x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
                 }
             } else {
+                // global columns: each lane loads BN/32 of this tile's positions, shuffles
+                // broadcast them; keep the ones outside the row's band
                 const int g0 = (j - n_band) * BN;
+                int gv[BN / 32];
+#pragma unroll
+                for (int i = 0; i < BN / 32; ++i) {
+                    const int gi = g0 + i * 32 + lane;
+                    gv[i] = gi < a.n_global ? __ldg(a.global_idx + gi) : -1;
+                }
+                int cnt4[4] = {0, 0, 0, 0};
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
-                    const int gi = g0 + c;
-                    bool al = false;
-                    if (gi < a.n_global) {
-                        const int gs = __ldg(a.global_idx + gi);
-                        al = gs >= 0 && gs < a.T && !in_band(t, gs, a.wl, a.wr);
-                    }
-                    count += al ? 1 : 0;
+                    const int gs = __shfl_sync(0xffffffffu, gv[c >> 5], c & 31);
+                    const bool al = (gs >= 0) & (gs < a.T) & ((gs < lo_abs) | (gs > hi_abs));
+                    cnt4[c & 3] += al ? 1 : 0;
                     x[c] = al ? x[c] : -INFINITY;
                 }
+                count += (cnt4[0] + cnt4[1]) + (cnt4[2] + cnt4[3]);
             }
             // ---- running max (log2 domain), tree reduction
             float mx8[8];
