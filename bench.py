@@ -300,6 +300,29 @@ class OracleSampler:
         return self.oracle.num_threads()
 
 
+def band_traffic_per_launch():
+    """DRAM bytes (read + write) of one band-kernel launch on the Mistral workload, from
+    the committed ncu summary -- only if it was captured from the current kernel source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "band_fwd_mistral_traffic.txt")
+    src = os.path.join(ROOT, "sliding_window_attention_swa_gb300", "csrc", "swa_band.cu")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if line.strip() and not line.startswith("#"):
+                    k, v = line.split(None, 1)
+                    fields[k] = v.strip()
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("kernel_source_sha256") != digest:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ----------------------------------------------------------------------------- main
 def load_peaks():
     try:
@@ -308,6 +331,25 @@ def load_peaks():
         return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, 1900.0, "fallback"
+
+
+def reduce_over_ranks(x: float, op: str, world: int, device) -> float:
+    """Max or sum of a per-rank scalar over all ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_rate(local_work: float, local_seconds: float, world: int, device) -> float:
+    """Whole-job throughput: the work all ranks processed / the slowest rank's time."""
+    total = reduce_over_ranks(local_work, "sum", world, device)
+    slowest = reduce_over_ranks(local_seconds, "max", world, device)
+    return total / slowest
 
 
 def dist_setup(n_gpus):
@@ -384,11 +426,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_over_ranks(x, "max", world, device)
 
     out = {}
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) if world == 1 else local
@@ -401,7 +439,7 @@ def main():
     clocks = cs.summary()
     ms = max_over_ranks(float(res["ms"].mean()))
     flops = res["flops"]
-    tflops = world * flops / (ms * 1e-3) / 1e12
+    tflops = job_rate(flops, float(res["ms"].mean()) * 1e-3, world, device) / 1e12
     kernel_tflops = flops / (float(res["ms"].mean()) * 1e-3) / 1e12
     e2e_ms, h2d, d2h = measure_e2e_prefill(I.MISTRAL, max(10, args.steps // 10), args.warmup, device, res["tensors"])
     e2e_ms = max_over_ranks(e2e_ms)
@@ -439,14 +477,7 @@ def main():
         cpu = {"value": v, "unit": "TFLOP/s", "cores": osamp.threads(), "kind": "oracle",
                "sample": f"{n} random query rows of the Mistral-shape workload ({dt:.1f} s, fp64)"}
 
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "band_fwd_mistral_traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                traffic = json.load(f).get("dram_bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = band_traffic_per_launch()
 
     if rank == 0:
         line = {
