@@ -150,6 +150,30 @@ SWA_API size_t swa_decode_workspace_size(const swa_decode_params *p);
 SWA_API swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t workspace_bytes,
                       swa_stream_t stream);
 
+/* Bytes of the built-in scratch array used by swa_decode_noalloc (16 MiB per device). */
+#define SWA_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * swa_decode without a caller-provided workspace, for callers that cannot allocate
+ * device memory where they call this: for example a serving loop that must not
+ * allocate once it is running (cudaMalloc can synchronise the device and can fail
+ * under memory pressure), or a plugin interface that hands the kernel only its
+ * inputs and outputs.  The paper has no counterpart; this is a library convenience.
+ *
+ * The split partials go to one fixed scratch array of SWA_DECODE_NOALLOC_SCRATCH_BYTES
+ * compiled into the library; every GPU that loads the library holds that array until
+ * the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called.  The first call on each device looks up the array's
+ * device address (with that device current) and caches it, so make that first call
+ * before any stream capture.  All calls on a device share the array and it keeps the
+ * previous call's contents (no part of it needs to start at zero); calls that overlap
+ * on the GPU -- on different streams or host threads -- race on it and must be
+ * serialised by the caller.  Parameters, layouts and results are those of swa_decode.
+ * Errors: as swa_decode; SWA_ERR_WORKSPACE when the problem needs more scratch than
+ * SWA_DECODE_NOALLOC_SCRATCH_BYTES (swa_decode_workspace_size(p) tells how much).
+ */
+SWA_API swa_status swa_decode_noalloc(const swa_decode_params *p, swa_stream_t stream);
+
 /*
  * Synchronises `stream`, then reads and clears the library's device error words.
  * Returns SWA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last

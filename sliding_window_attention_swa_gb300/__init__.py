@@ -93,6 +93,8 @@ def load_library(path: str | None = None):
     lib.swa_decode_workspace_size.restype = sz
     lib.swa_decode.argtypes = [ctypes.POINTER(SwaDecodeParams), vp, sz, vp]
     lib.swa_decode.restype = ctypes.c_int
+    lib.swa_decode_noalloc.argtypes = [ctypes.POINTER(SwaDecodeParams), vp]
+    lib.swa_decode_noalloc.restype = ctypes.c_int
     lib.swa_check_device_error.argtypes = [vp]
     lib.swa_check_device_error.restype = ctypes.c_int
     lib.swa_last_error_string.argtypes = []

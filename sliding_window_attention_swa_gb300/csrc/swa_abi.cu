@@ -70,6 +70,9 @@ swa_status workspace_ok(void *ws, size_t have, size_t need) {
 
 }  // namespace
 
+swa_status swa::validate_decode(const swa_decode_params *p) { return decode_check(p); }
+bool swa::record_cuda_failure(cudaError_t e) { return failed(e); }
+
 extern "C" {
 
 int32_t swa_abi_version(void) { return SWA_ABI_VERSION; }

@@ -96,6 +96,10 @@ struct BandArgs {
     int32_t *counts;
 };
 cudaError_t launch_band(const BandArgs &a, cudaStream_t s);
+
+// Host-side helpers of the C ABI shared with the allocation-free decode entry point.
+swa_status validate_decode(const swa_decode_params *p);  // the checks swa_decode applies
+bool record_cuda_failure(cudaError_t e);                  // true (and recorded) if e failed
 unsigned int band_read_clear_error();
 
 }  // namespace swa
