@@ -64,14 +64,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up (returns false)
-// when *abort becomes non-zero (another role of the CTA gave up) or after
-// kWaitLimitNs, in which case it raises *abort and ORs kErrWaitTimeout into err.
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Spins on the
+// non-blocking test first (a suspended try_wait can wake late), then polls with
+// try_wait.  Gives up (returns false) when *abort becomes non-zero (another role
+// of the CTA gave up) or after kWaitLimitNs, in which case it raises *abort and
+// ORs kErrWaitTimeout into err.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           unsigned int *err) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 4096; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {

@@ -263,7 +263,7 @@ swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t worksp
 
 swa_status swa_check_device_error(swa_stream_t stream) {
     if (failed(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)))) return SWA_ERR_CUDA;
-    const unsigned int e = swa::band_read_clear_error();
+    const unsigned int e = swa::band_read_clear_error() | swa::split_read_clear_error();
     return e ? SWA_ERR_TIMEOUT : SWA_OK;
 }
 

@@ -81,6 +81,7 @@ inline void split_carve(void *ws, int B, int NQ, int H_q, int H_kv, int D, int n
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+unsigned int split_read_clear_error();
 
 // Banded prefill (tcgen05 path).
 struct BandArgs {

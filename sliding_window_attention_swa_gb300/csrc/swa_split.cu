@@ -2,18 +2,34 @@
 // slots, and the log-sum-exp merge of the splits.
 //
 // Used for ring-buffer decode (one query token per sequence against its W cache
-// slots, validity from the stored slot positions) and for the global rows of the
-// prefill path (each global position attends to all T keys).  Work is
-// HBM-bound: every valid key/value byte is read once.  A CTA owns 512 slots of
-// one (batch, kv head, query block); 4 warps share a cp.async pipeline of
-// 64-slot chunks (K and V, XOR-swizzled rows) and each warp scores 16 slots of
-// every chunk with mma.sync (the query block's <= 16 rows -- a GQA group of
-// heads -- are the M dimension).  Chunks without a valid slot are never loaded;
-// invalid slots inside a loaded chunk are zero-filled, so uninitialised cache
-// memory cannot leak into the result.  Each split writes (max, sum, weighted
-// values); the merge kernel combines them (FlashAttention-style rescaling).
+// slots; a slot is valid when its stored position lies in the query's window,
+// Gemma 3 note, ai-engineer-exhaustive.pages.dev "How it works") and for the
+// global rows of the prefill path (each global position attends to all T keys,
+// prathamp.com "Sliding Window Attention: From Local Windows to Global Context",
+// section 4.3).  The work is HBM-bound: every valid key/value byte is read once.
+//
+// Persistent kernel, one CTA per SM, five warps:
+//   warp 0     producer.  Walks this CTA's work items (batch, kv head, query block,
+//              512-slot split) in a static round-robin order.  For each item it
+//              reads the slot positions, builds one 64-bit validity mask per
+//              64-slot chunk, writes the split's valid count, and streams the K and
+//              V of every chunk that has a valid slot into a ring of NST stages
+//              with TMA (128B swizzle); chunks without a valid slot are never read.
+//   warps 1-4  consumers.  Each scores 16 slots of every chunk with mma.sync (the
+//              query block's <= 16 rows -- a GQA group of heads -- are the M
+//              dimension), keeps a running (max, sum, weighted values) per row, and
+//              at the end of an item the four warps combine through shared memory
+//              and write the split's partial.  Value rows of invalid slots are
+//              zeroed before P V, so whatever an unwritten slot holds (even NaN)
+//              never reaches the result.
+// The merge kernel combines the splits of a row (FlashAttention-style rescaling).
+// Every wait is bounded; on expiry the CTA records an error word, drains its
+// copies and returns.
 #include <cfloat>
+#include <climits>
 #include <cmath>
+
+#include <cudaTypedefs.h>
 
 #include "ptx.cuh"
 #include "swa_internal.h"
@@ -21,296 +37,400 @@
 namespace swa {
 namespace {
 
-template <int D>
-struct SplitCfg {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kPieces = D / 8;  // 16-byte pieces per row
-    static constexpr int kTileBytes = kSplitChunk * kRowBytes;
-    static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 3 : 2);
-    static constexpr int kSmem = kStages * 2 * kTileBytes;
-    static_assert(kSmem >= 4 * kSplitRows * D * 4, "combine buffer must fit in the stage memory");
+__device__ unsigned int g_split_err = 0;
+
+constexpr int CH = kSplitChunk;                 // slots per chunk (64)
+constexpr int MAX_CHUNKS = kSlotsPerSplit / CH;  // chunks per split (8)
+constexpr int kThreads = 160;
+
+struct StageHdr {
+    int item, chunk, last, pad;
+    unsigned long long mask;  // bit i: slot chunk*64 + i of the split is valid
+    unsigned long long pad2;
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int piece, int row_bytes) {
-    return static_cast<uint32_t>(row * row_bytes + ((piece ^ (row & 7)) << 4));
+// Two CTAs share an SM where the shared memory allows (head dim <= 128), so one
+// CTA's end-of-item combine overlaps the other's streaming; two or more 32 KB
+// stages in flight per CTA keep HBM busy.
+template <int D>
+struct StreamCfg {
+    static constexpr int STAGE = 2 * CH * D * 2;        // K + V of one chunk
+    static constexpr int CBUF = 4 * kSplitRows * D * 4;  // combine buffer [4 warps][16 rows][D] fp32
+    static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
+    static constexpr int NST_RAW = (232448 / CTAS_PER_SM - 2048 - CBUF) / STAGE;
+    static constexpr int NST = NST_RAW > 8 ? 8 : NST_RAW;
+    static constexpr int OFF_RING = 0;
+    static constexpr int OFF_CBUF = NST * STAGE;
+    static constexpr int OFF_HDR = OFF_CBUF + CBUF;
+    static constexpr int OFF_RED = OFF_HDR + NST * static_cast<int>(sizeof(StageHdr));  // red_m, red_l [4][16]
+    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * kSplitRows * 4;
+    // full[NST], empty[NST], cmb_full, cmb_done
+    static constexpr int NBAR = 2 * NST + 2;
+    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;
+    static_assert(NST >= 2, "ring too shallow");
+    static_assert(SMEM * CTAS_PER_SM <= 232448, "shared memory budget");
+};
+
+// Offset of 16-byte piece `pc` of row `row` in a 128B-swizzled tile of `rows` rows
+// written by TMA boxes of 64 elements (one 128-byte row per box row).
+__device__ __forceinline__ uint32_t sw128(int rows, int row, int pc) {
+    return static_cast<uint32_t>((pc >> 3) * (rows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4));
 }
 
+struct StreamKernelArgs {
+    SplitArgs s;
+    int n_items;
+    int nqb;
+};
+
+// Registers: two 5-warp CTAs put three warps on two of the SM's sub-partitions,
+// whose 16K-register files then allow at most 168 registers a thread.
 template <int D>
-__global__ void __launch_bounds__(128) split_attn_kernel(const SplitArgs a) {
-    using C = SplitCfg<D>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ uint8_t valid[kSlotsPerSplit];
-    __shared__ int chunk_list[kSlotsPerSplit / kSplitChunk];
-    __shared__ int n_chunks_valid;
-    __shared__ int cnt_total;
-    __shared__ float red_m[4][kSplitRows];
-    __shared__ float red_l[4][kSplitRows];
+__global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
+    stream_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const StreamKernelArgs ka) {
+    using C = StreamCfg<D>;
+    constexpr int NST = C::NST;
+    const SplitArgs &a = ka.s;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int abort_flag;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int split = blockIdx.x;
-    const int nqb = (a.NQ + a.q_per_cta - 1) / a.q_per_cta;
-    const int kvh = blockIdx.y / nqb, qb = blockIdx.y % nqb;
-    const int b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sraw = smem_u32(smem_raw);
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    uint8_t *sgen = smem_raw + (sbase - sraw);
+    StageHdr *hdr = reinterpret_cast<StageHdr *>(sgen + C::OFF_HDR);
+    float *cbuf = reinterpret_cast<float *>(sgen + C::OFF_CBUF);
+    float *red_m = reinterpret_cast<float *>(sgen + C::OFF_RED);
+    float *red_l = red_m + 4 * kSplitRows;
+    const uint32_t bars = sbase + C::OFF_BAR;
+    auto bar_full = [&](int s) { return bars + 8u * s; };
+    auto bar_empty = [&](int s) { return bars + 8u * (NST + s); };
+    const uint32_t bar_cf = bars + 8u * (2 * NST), bar_cd = bars + 8u * (2 * NST + 1);
     const int group = a.H_q / a.H_kv;
-    const int slot0 = split * a.slots_per_split;
-    const int nslots = min(a.n_slots, slot0 + a.slots_per_split) - slot0;
+    const int Y = a.H_kv * ka.nqb;
 
-    // ---- 1. slot validity, valid count, and the list of chunks worth loading
     if (tid == 0) {
-        cnt_total = 0;
-        n_chunks_valid = 0;
-    }
-    __syncthreads();
-    {
-        const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[b]) : 0;
-        int mine = 0;
-        for (int i = tid; i < a.slots_per_split; i += 128) {
-            bool ok = false;
-            if (i < nslots) {
-                if (a.slot_pos) {
-                    const int64_t p = a.slot_pos[static_cast<int64_t>(b) * a.W + slot0 + i];
-                    ok = p >= 0 && p > t - a.W && p <= t;
-                } else {
-                    ok = true;
-                }
-            }
-            valid[i] = ok ? 1 : 0;
-            mine += ok ? 1 : 0;
+        abort_flag = 0;
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar_full(s), 1);
+            mbar_init(bar_empty(s), 4);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-        if (lane == 0) atomicAdd(&cnt_total, mine);
+        mbar_init(bar_cf, 4);
+        mbar_init(bar_cd, 4);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
     __syncthreads();
+    volatile int *abort = &abort_flag;
+
     if (warp == 0) {
-        const int nch = (nslots + kSplitChunk - 1) / kSplitChunk;
-        for (int c0 = 0; c0 < nch; c0 += 32) {
-            const int c = c0 + lane;
-            bool any = false;
-            if (c < nch)
-                for (int i = 0; i < kSplitChunk; ++i) any |= valid[c * kSplitChunk + i] != 0;
-            const unsigned m = __ballot_sync(0xffffffffu, any);
-            if (any) chunk_list[n_chunks_valid + __popc(m & ((1u << lane) - 1u))] = c;
-            __syncwarp();
-            if (lane == 0) n_chunks_valid += __popc(m);
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    const int nvc = n_chunks_valid;
-
-    // ---- 2. query fragments (rows r0 = lane/4, r1 = r0 + 8 of the 16-row M tile)
-    const int rows = a.q_per_cta * group;
-    uint32_t qa[D / 16][4];
-    {
-        const int rr[2] = {lane >> 2, (lane >> 2) + 8};
-        const __nv_bfloat16 *qp[2];
-        bool rv[2];
+        // ============================ producer ============================
+        int seq = 0;          // stages emitted so far
+        bool ok = true;
+        // Slot positions of an item, 16 per lane (slot i*32 + lane of the split); the
+        // loads for item i + grid are issued before item i's chunks are streamed.
+        auto load_pos = [&](int item, int (&pv)[2 * MAX_CHUNKS]) {
+            if (item >= ka.n_items) return;
+            const int split = item % a.n_splits;
+            const int b = item / (a.n_splits * Y);
+            const int slot0 = split * a.slots_per_split;
+            const int nslots = min(a.n_slots, slot0 + a.slots_per_split) - slot0;
+            const int32_t *row = a.slot_pos ? a.slot_pos + static_cast<int64_t>(b) * a.W + slot0 : nullptr;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = rr[i];
-            const int qs = qb * a.q_per_cta + r / group;
-            rv[i] = r < rows && qs < a.NQ;
-            const int h = kvh * group + r % group;
-            int64_t tok = (rv[i] && a.q_tok) ? a.q_tok[qs] : 0;
-            if (tok < 0 || tok >= a.tok_limit) {
-                rv[i] = false;
-                tok = 0;
+            for (int i = 0; i < 2 * MAX_CHUNKS; ++i) {
+                const int si = i * 32 + lane;
+                pv[i] = si >= nslots ? INT_MIN : (row ? __ldg(row + si) : 0);
             }
-            qp[i] = static_cast<const __nv_bfloat16 *>(a.q) + static_cast<int64_t>(b) * a.q_sb + tok * a.q_st +
-                    static_cast<int64_t>(h) * a.q_sh;
-        }
-        const int c = 2 * (lane & 3);
+        };
+        int pos_cur[2 * MAX_CHUNKS], pos_next[2 * MAX_CHUNKS];
+        load_pos(blockIdx.x, pos_cur);
+        for (int item = blockIdx.x; item < ka.n_items && ok; item += gridDim.x) {
+            const int split = item % a.n_splits;
+            const int y = (item / a.n_splits) % Y;
+            const int b = item / (a.n_splits * Y);
+            const int kvh = y / ka.nqb, qb = y % ka.nqb;
+            const int slot0 = split * a.slots_per_split;
+            const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[b]) : 0;
+            load_pos(item + gridDim.x, pos_next);
+            // validity of the item's slots, 64 per chunk (two ballots)
+            bool v[2 * MAX_CHUNKS];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qa[kk][0] = rv[0] ? *reinterpret_cast<const uint32_t *>(qp[0] + kk * 16 + c) : 0u;
-            qa[kk][1] = rv[1] ? *reinterpret_cast<const uint32_t *>(qp[1] + kk * 16 + c) : 0u;
-            qa[kk][2] = rv[0] ? *reinterpret_cast<const uint32_t *>(qp[0] + kk * 16 + 8 + c) : 0u;
-            qa[kk][3] = rv[1] ? *reinterpret_cast<const uint32_t *>(qp[1] + kk * 16 + 8 + c) : 0u;
-        }
-    }
-
-    // ---- 3. pipelined loop over the valid chunks
-    const uint32_t sbase = smem_u32(smem);
-    const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(a.k) + static_cast<int64_t>(b) * a.k_sb +
-                              static_cast<int64_t>(kvh) * a.k_sh;
-    const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(a.v) + static_cast<int64_t>(b) * a.v_sb +
-                              static_cast<int64_t>(kvh) * a.v_sh;
-
-    auto issue = [&](int stage, int chunk) {
-        const uint32_t kdst = sbase + stage * 2 * C::kTileBytes;
-        const uint32_t vdst = kdst + C::kTileBytes;
-        constexpr int kPer = kSplitChunk * C::kPieces;  // pieces per tile
-#pragma unroll 4
-        for (int idx = tid; idx < kPer; idx += 128) {
-            const int r = idx / C::kPieces, pc = idx % C::kPieces;
-            const int si = chunk * kSplitChunk + r;  // slot index within the split
-            const bool ok = si < nslots && valid[si];
-            const int64_t slot = ok ? slot0 + si : slot0;
-            const uint32_t o = swz(r, pc, C::kRowBytes);
-            cp_async16(kdst + o, kb + slot * a.k_ss + pc * 8, ok);
-            cp_async16(vdst + o, vb + slot * a.v_ss + pc * 8, ok);
-        }
-    };
-
+            for (int i = 0; i < 2 * MAX_CHUNKS; ++i) {
+                const int64_t p = pos_cur[i];
+                v[i] = pos_cur[i] != INT_MIN && (!a.slot_pos || (p >= 0 && p > t - a.W && p <= t));
+            }
+            unsigned long long mask[MAX_CHUNKS];
+            int count = 0;
 #pragma unroll
-    for (int s = 0; s < C::kStages - 1; ++s) {
-        if (s < nvc) issue(s, chunk_list[s]);
-        cp_async_commit();
-    }
-
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float acc[D / 8][4];
+            for (int c = 0; c < MAX_CHUNKS; ++c) {
+                const unsigned lo = __ballot_sync(0xffffffffu, v[2 * c]);
+                const unsigned hi = __ballot_sync(0xffffffffu, v[2 * c + 1]);
+                mask[c] = static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
+                count += __popcll(mask[c]);
+            }
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-
+            for (int i = 0; i < 2 * MAX_CHUNKS; ++i) pos_cur[i] = pos_next[i];
+            if (qb == 0 && lane == 0)
+                a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_splits + split] = count;
+            int last_c = -1;
+#pragma unroll
+            for (int c = 0; c < MAX_CHUNKS; ++c)
+                if (mask[c]) last_c = c;
+            // emit the chunks with a valid slot (one empty stage if there is none)
 #pragma unroll 1
-    for (int i = 0; i < nvc; ++i) {
-        cp_async_wait<C::kStages - 2>();
-        __syncthreads();
-        {
-            const int nx = i + C::kStages - 1;
-            if (nx < nvc) issue(nx % C::kStages, chunk_list[nx]);
-            cp_async_commit();
-        }
-        const int stage = i % C::kStages;
-        const int chunk = chunk_list[i];
-        const uint32_t ks = sbase + stage * 2 * C::kTileBytes;
-        const uint32_t vs = ks + C::kTileBytes;
-
-        // S = Q K^T for this warp's 16 slots (two n-tiles of 8)
-        float sc[2][4];
+            for (int c = 0; c < MAX_CHUNKS && ok; ++c) {
+                const bool emit = mask[c] != 0 || (last_c < 0 && c == 0);
+                if (!emit) continue;
+                const int st = seq % NST;
+                if (seq >= NST) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    StageHdr &h = hdr[st];
+                    h.item = item;
+                    h.chunk = c;
+                    h.last = (c == last_c || last_c < 0) ? 1 : 0;
+                    h.mask = mask[c];
+                    if (mask[c]) {
+                        const uint32_t kd = sbase + C::OFF_RING + st * C::STAGE;
+                        const uint32_t vd = kd + C::STAGE / 2;
+                        mbar_arrive_expect_tx(bar_full(st), C::STAGE);
+                        const int srow = slot0 + c * CH;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            const int row = 16 * warp + 8 * nt + (lane & 7);
-#pragma unroll
-            for (int k2 = 0; k2 < D / 32; ++k2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(ks + swz(row, k2 * 4 + (lane >> 3), C::kRowBytes), b0, b1, b2, b3);
-                mma_bf16_16816(sc[nt], qa[2 * k2], b0, b1);
-                mma_bf16_16816(sc[nt], qa[2 * k2 + 1], b2, b3);
+                        for (int pc = 0; pc < D / 64; ++pc) {
+                            tma_load_4d(kd + pc * (CH * 128), &tm_k, bar_full(st), pc * 64, srow, kvh, b);
+                            tma_load_4d(vd + pc * (CH * 128), &tm_v, bar_full(st), pc * 64, srow, kvh, b);
+                        }
+                    } else {
+                        mbar_arrive(bar_full(st));
+                    }
+                }
+                __syncwarp();
+                ++seq;
             }
         }
-        // mask + scale (log2 domain)
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int si = chunk * kSplitChunk + 16 * warp + 8 * nt + 2 * (lane & 3) + (e & 1);
-                const bool ok = si < nslots && valid[si];
-                sc[nt][e] = ok ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        if (!ok && lane == 0) {
+            // drain the copies still in flight (at most the last NST stages)
+            for (int s = max(0, seq - NST); s < seq; ++s) mbar_drain(bar_full(s % NST), (s / NST) & 1, &g_split_err);
+        }
+    } else {
+        // ============================ consumers ============================
+        const int w = warp - 1;  // slots [16w, 16w + 16) of every chunk
+        const int rows = a.q_per_cta * group;
+        const int r0 = lane >> 2, r1 = r0 + 8;
+        const int kq = 2 * (lane & 3);
+        uint32_t qa[D / 16][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float acc[D / 8][4];
+        int cur = -1, n_done = 0;
+        bool ok = true;
+#pragma unroll 1
+        for (int seq = 0; ok; ++seq) {
+            const int st = seq % NST;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (seq / NST) & 1, abort, &g_split_err))) {
+                ok = false;
+                break;
             }
-            mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-        }
+            const int item = hdr[st].item, chunk = hdr[st].chunk, last = hdr[st].last;
+            const unsigned long long mask = hdr[st].mask;
+            const int split = item % a.n_splits;
+            const int y = (item / a.n_splits) % Y;
+            const int b = item / (a.n_splits * Y);
+            const int kvh = y / ka.nqb, qb = y % ka.nqb;
+            if (item != cur) {
+                // new item: query fragments of its rows (r0, r1 of the 16-row M tile), fresh state
+                cur = item;
+                const int rr[2] = {r0, r1};
+                const __nv_bfloat16 *qp[2];
+                bool rv[2];
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
-        const float al1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        float p[2][4];
-        float s0 = 0.f, s1 = 0.f;
+                for (int i = 0; i < 2; ++i) {
+                    const int r = rr[i];
+                    const int qs = qb * a.q_per_cta + r / group;
+                    rv[i] = r < rows && qs < a.NQ;
+                    int64_t tok = (rv[i] && a.q_tok) ? a.q_tok[qs] : 0;
+                    if (tok < 0 || tok >= a.tok_limit) {
+                        rv[i] = false;
+                        tok = 0;
+                    }
+                    const int h = kvh * group + r % group;
+                    qp[i] = static_cast<const __nv_bfloat16 *>(a.q) + static_cast<int64_t>(b) * a.q_sb + tok * a.q_st +
+                            static_cast<int64_t>(h) * a.q_sh;
+                }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            p[nt][0] = mn0 == -INFINITY ? 0.f : ex2(sc[nt][0] - mn0);
-            p[nt][1] = mn0 == -INFINITY ? 0.f : ex2(sc[nt][1] - mn0);
-            p[nt][2] = mn1 == -INFINITY ? 0.f : ex2(sc[nt][2] - mn1);
-            p[nt][3] = mn1 == -INFINITY ? 0.f : ex2(sc[nt][3] - mn1);
-            s0 += p[nt][0] + p[nt][1];
-            s1 += p[nt][2] + p[nt][3];
-        }
-        l0 = l0 * al0 + s0;
-        l1 = l1 * al1 + s1;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    qa[kk][0] = rv[0] ? __ldg(reinterpret_cast<const unsigned *>(qp[0] + kk * 16 + kq)) : 0u;
+                    qa[kk][1] = rv[1] ? __ldg(reinterpret_cast<const unsigned *>(qp[1] + kk * 16 + kq)) : 0u;
+                    qa[kk][2] = rv[0] ? __ldg(reinterpret_cast<const unsigned *>(qp[0] + kk * 16 + 8 + kq)) : 0u;
+                    qa[kk][3] = rv[1] ? __ldg(reinterpret_cast<const unsigned *>(qp[1] + kk * 16 + 8 + kq)) : 0u;
+                }
+                m0 = m1 = -INFINITY;
+                l0 = l1 = 0.f;
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            acc[n][0] *= al0;
-            acc[n][1] *= al0;
-            acc[n][2] *= al1;
-            acc[n][3] *= al1;
-        }
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-        pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-        pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-        pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-        // O += P V (V^T fragments via transposing ldmatrix)
-        const int vrow = 16 * warp + 8 * ((lane >> 3) & 1) + (lane & 7);
+                for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            }
+            const unsigned wmask = static_cast<unsigned>(mask >> (16 * w)) & 0xffffu;  // this warp's 16 slots
+            if (wmask) {
+                const uint32_t ks = sbase + C::OFF_RING + st * C::STAGE;
+                const uint32_t vs = ks + C::STAGE / 2;
+                if (wmask != 0xffffu) {
+                    // zero the value rows of this warp's invalid slots
+                    uint8_t *vg = sgen + C::OFF_RING + st * C::STAGE + C::STAGE / 2;
+                    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+                        const int rr = idx / (D / 8), pc = idx % (D / 8);
+                        if (!((wmask >> rr) & 1u))
+                            *reinterpret_cast<uint4 *>(vg + sw128(CH, 16 * w + rr, pc)) = make_uint4(0, 0, 0, 0);
+                    }
+                    __syncwarp();
+                }
+                // S = Q K^T over this warp's 16 slots (two n-tiles of 8)
+                float sc[2][4];
 #pragma unroll
-        for (int d2 = 0; d2 < D / 16; ++d2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vs + swz(vrow, 2 * d2 + (lane >> 4), C::kRowBytes), b0, b1, b2, b3);
-            mma_bf16_16816(acc[2 * d2], pa, b0, b1);
-            mma_bf16_16816(acc[2 * d2 + 1], pa, b2, b3);
-        }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
+                for (int nt = 0; nt < 2; ++nt) {
+                    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    const int row = 16 * w + 8 * nt + (lane & 7);
+#pragma unroll
+                    for (int k2 = 0; k2 < D / 32; ++k2) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(ks + sw128(CH, row, k2 * 4 + (lane >> 3)), b0, b1, b2, b3);
+                        mma_bf16_16816(sc[nt], qa[2 * k2], b0, b1);
+                        mma_bf16_16816(sc[nt], qa[2 * k2 + 1], b2, b3);
+                    }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int bit = 8 * nt + kq + (e & 1);
+                        sc[nt][e] = ((wmask >> bit) & 1u) ? sc[nt][e] * a.scale_log2 : -INFINITY;
+                    }
+                    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+                }
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float al0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
+                const float al1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                float p[2][4];
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    p[nt][0] = mn0 == -INFINITY ? 0.f : ex2(sc[nt][0] - mn0);
+                    p[nt][1] = mn0 == -INFINITY ? 0.f : ex2(sc[nt][1] - mn0);
+                    p[nt][2] = mn1 == -INFINITY ? 0.f : ex2(sc[nt][2] - mn1);
+                    p[nt][3] = mn1 == -INFINITY ? 0.f : ex2(sc[nt][3] - mn1);
+                    s0 += p[nt][0] + p[nt][1];
+                    s1 += p[nt][2] + p[nt][3];
+                }
+                l0 = l0 * al0 + s0;
+                l1 = l1 * al1 + s1;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    acc[n][0] *= al0;
+                    acc[n][1] *= al0;
+                    acc[n][2] *= al1;
+                    acc[n][3] *= al1;
+                }
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+                pa[1] = pack_bf16x2(p[0][2], p[0][3]);
+                pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+                pa[3] = pack_bf16x2(p[1][2], p[1][3]);
+                // O += P V (V^T fragments via transposing ldmatrix)
+                const int vrow = 16 * w + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+                for (int d2 = 0; d2 < D / 16; ++d2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vs + sw128(CH, vrow, 2 * d2 + (lane >> 4)), b0, b1, b2, b3);
+                    mma_bf16_16816(acc[2 * d2], pa, b0, b1);
+                    mma_bf16_16816(acc[2 * d2 + 1], pa, b2, b3);
+                }
+                // order this warp's generic writes (zeroed rows) before the next TMA into the stage
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty(st));
+            (void)chunk;
 
-    // ---- 4. combine the 4 warps, write this split's partial result
+            if (last) {
+                // ---- combine the four warps and write this split's partial
+                float ls0 = l0, ls1 = l1;
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    const int r0 = lane >> 2, r1 = r0 + 8;
-    if ((lane & 3) == 0) {
-        red_m[warp][r0] = m0;
-        red_m[warp][r1] = m1;
-        red_l[warp][r0] = l0;
-        red_l[warp][r1] = l1;
-    }
-    __syncthreads();
-    float *cbuf = reinterpret_cast<float *>(smem);  // [4][16][D]
-    {
-        float mw0 = -INFINITY, mw1 = -INFINITY;
+                for (int o = 1; o <= 2; o <<= 1) {
+                    ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+                    ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
+                }
+                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_cd, (n_done - 1) & 1, abort, &g_split_err))) {
+                    ok = false;
+                    break;
+                }
+                if ((lane & 3) == 0) {
+                    red_m[w * kSplitRows + r0] = m0;
+                    red_m[w * kSplitRows + r1] = m1;
+                    red_l[w * kSplitRows + r0] = ls0;
+                    red_l[w * kSplitRows + r1] = ls1;
+                }
+                if (r0 < rows) {
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            mw0 = fmaxf(mw0, red_m[w][r0]);
-            mw1 = fmaxf(mw1, red_m[w][r1]);
+                    for (int n = 0; n < D / 8; ++n)
+                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r0) * D + 8 * n + kq) =
+                            make_float2(acc[n][0], acc[n][1]);
+                }
+                if (r1 < rows) {
+#pragma unroll
+                    for (int n = 0; n < D / 8; ++n)
+                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r1) * D + 8 * n + kq) =
+                            make_float2(acc[n][2], acc[n][3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_cf);
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_cf, n_done & 1, abort, &g_split_err))) {
+                    ok = false;
+                    break;
+                }
+                for (int idx = w * 32 + lane; idx < rows * D; idx += 128) {
+                    const int r = idx / D, d = idx % D;
+                    const int qs = qb * a.q_per_cta + r / group;
+                    if (qs >= a.NQ) continue;
+                    if (a.q_tok && (a.q_tok[qs] < 0 || a.q_tok[qs] >= a.tok_limit)) continue;
+                    const int h = kvh * group + r % group;
+                    float mw = -INFINITY;
+#pragma unroll
+                    for (int ww = 0; ww < 4; ++ww) mw = fmaxf(mw, red_m[ww * kSplitRows + r]);
+                    float s = 0.f, L = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < 4; ++ww) {
+                        const float f = mw == -INFINITY ? 0.f : ex2(red_m[ww * kSplitRows + r] - mw);
+                        s += cbuf[(ww * kSplitRows + r) * D + d] * f;
+                        L += red_l[ww * kSplitRows + r] * f;
+                    }
+                    const int64_t row = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits + split;
+                    a.ws_acc[row * D + d] = s;
+                    if (d == 0) {
+                        a.ws_ml[row * 2 + 0] = mw;
+                        a.ws_ml[row * 2 + 1] = L;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_cd);
+                ++n_done;
+                cur = -1;
+                if (item + static_cast<int>(gridDim.x) >= ka.n_items) break;  // this CTA's last item
+            }
         }
-        const float f0 = mw0 == -INFINITY ? 0.f : ex2(m0 - mw0);
-        const float f1 = mw1 == -INFINITY ? 0.f : ex2(m1 - mw1);
-        float *c0 = cbuf + (warp * kSplitRows + r0) * D;
-        float *c1 = cbuf + (warp * kSplitRows + r1) * D;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            const int d = 8 * n + 2 * (lane & 3);
-            *reinterpret_cast<float2 *>(c0 + d) = make_float2(acc[n][0] * f0, acc[n][1] * f0);
-            *reinterpret_cast<float2 *>(c1 + d) = make_float2(acc[n][2] * f1, acc[n][3] * f1);
-        }
     }
-    __syncthreads();
-    for (int idx = tid; idx < rows * D; idx += 128) {
-        const int r = idx / D, d = idx % D;
-        const int qs = qb * a.q_per_cta + r / group;
-        if (qs >= a.NQ) continue;
-        if (a.q_tok && (a.q_tok[qs] < 0 || a.q_tok[qs] >= a.tok_limit)) continue;
-        const int h = kvh * group + r % group;
-        float mw = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) mw = fmaxf(mw, red_m[w][r]);
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) s += cbuf[(w * kSplitRows + r) * D + d];
-        const int64_t row = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits + split;
-        a.ws_acc[row * D + d] = s;
-        if (d == 0) {
-            float L = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                L += mw == -INFINITY ? 0.f : red_l[w][r] * ex2(red_m[w][r] - mw);
-            a.ws_ml[row * 2 + 0] = mw;
-            a.ws_ml[row * 2 + 1] = L;
-        }
-    }
-    if (qb == 0 && tid == 0) a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_splits + split] = cnt_total;
 }
 
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
@@ -346,18 +466,74 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 4-D bf16 map over (d, slot, kv head, batch) -- any element strides -- with a
+// (64, 64, 1, 1) box and 128-B swizzle.
+bool slot_map(CUtensorMap *m, const void *base, int D, int n_slots, int H, int B, int64_t s_slot, int64_t s_head,
+              int64_t s_batch) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_slots), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_slot) * 2, static_cast<cuuint64_t>(s_head) * 2,
+                             static_cast<cuuint64_t>(s_batch) * 2};
+    cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(CH), 1u, 1u};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int n[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!n[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
 template <int D>
-cudaError_t launch_split_d(const SplitArgs &a, cudaStream_t s) {
-    using C = SplitCfg<D>;
-    static bool configured = false;  // idempotent attribute set; benign if raced
+cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
+    using C = StreamCfg<D>;
+    static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(split_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(stream_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int nqb = (a.NQ + a.q_per_cta - 1) / a.q_per_cta;
-    dim3 grid(a.n_splits, a.H_kv * nqb, a.B);
-    split_attn_kernel<D><<<grid, 128, C::kSmem, s>>>(a);
+    if (a.slots_per_split != kSlotsPerSplit) return cudaErrorInvalidValue;
+    CUtensorMap mk, mv;
+    if (!slot_map(&mk, a.k, D, a.n_slots, a.H_kv, a.B, a.k_ss, a.k_sh, a.k_sb) ||
+        !slot_map(&mv, a.v, D, a.n_slots, a.H_kv, a.B, a.v_ss, a.v_sh, a.v_sb))
+        return cudaErrorInvalidValue;
+    StreamKernelArgs ka{};
+    ka.s = a;
+    ka.nqb = (a.NQ + a.q_per_cta - 1) / a.q_per_cta;
+    const long long items = static_cast<long long>(a.B) * a.H_kv * ka.nqb * a.n_splits;
+    if (items <= 0 || items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    ka.n_items = static_cast<int>(items);
+    const int slots = sm_count() * C::CTAS_PER_SM;
+    const int grid = static_cast<int>(items < slots ? items : slots);
+    stream_attn_kernel<D><<<grid, kThreads, C::SMEM, s>>>(mk, mv, ka);
     return cudaGetLastError();
 }
 
@@ -365,9 +541,9 @@ cudaError_t launch_split_d(const SplitArgs &a, cudaStream_t s) {
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_split_d<64>(a, s);
-        case 128: return launch_split_d<128>(a, s);
-        case 256: return launch_split_d<256>(a, s);
+        case 64: return launch_stream_d<64>(a, s);
+        case 128: return launch_stream_d<128>(a, s);
+        case 256: return launch_stream_d<256>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -376,6 +552,13 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s) {
     dim3 grid(a.NQ * a.H_q, a.B);
     merge_kernel<<<grid, 128, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+unsigned int split_read_clear_error() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_split_err, sizeof v) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_split_err, &z, sizeof z);
+    return v;
 }
 
 }  // namespace swa
