@@ -77,16 +77,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Spins on the
-// non-blocking test first (a suspended try_wait can wake late), then polls with
-// try_wait.  Gives up (returns false) when *abort becomes non-zero (another role
-// of the CTA gave up) or after kWaitLimitNs, in which case it raises *abort and
-// ORs kErrWaitTimeout into err.
+// Waits for the phase with the given parity to complete.  kSpin: spin on the
+// non-blocking test first (for warps with nothing else to do on their SM
+// sub-partition; a suspended try_wait can wake late); otherwise poll with
+// try_wait, which lets the warp sleep and leaves issue slots to its neighbours.
+// Gives up (returns false) when *abort becomes non-zero (another role of the CTA
+// gave up) or after kWaitLimitNs, in which case it raises *abort and ORs
+// kErrWaitTimeout into err.
+template <bool kSpin = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           unsigned int *err) {
+    if constexpr (kSpin) {
 #pragma unroll 1
-    for (int i = 0; i < 4096; ++i)
-        if (mbar_test_wait(bar, parity)) return true;
+        for (int i = 0; i < 4096; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
+    } else {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+    }
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {

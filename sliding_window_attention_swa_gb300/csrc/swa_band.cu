@@ -14,20 +14,24 @@
 // (prathamp.com "Sliding Window Attention: From Local Windows to Global Context",
 // section 4.3).
 //
+// Persistent: one CTA per SM walks the units (longest first, round-robin); TMEM and
+// the mbarriers are set up once and every barrier phase runs on across units.
 // Roles:
-//   warp 0        producer: Q tiles once (TMA); then K_0, V_0, K_1, V_1, ... into
-//                 a ring of NSLOT shared-memory slots (TMA for band tiles, plain
-//                 gathers into the same 128B-swizzled layout for global tiles).
+//   warp 0        K/V producer: K_0, V_0, K_1, V_1, ... of every unit into a ring of
+//                 NSLOT shared-memory slots (TMA for band tiles, plain gathers into
+//                 the same 128B-swizzled layout for global tiles).
 //   warp 1        TMEM owner and MMA issuer (one thread):
 //                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
-//   warps 2..     NQT softmax warpgroups; one row per thread (TMEM lane).  Scores
-//                 are masked only on band-edge and global tiles; the running max is
-//                 kept in the log2 domain; P = 2^(x - m) is written back as bf16 over
-//                 the S columns it came from; O is rescaled in TMEM only when a row's
-//                 max grows by more than 2^8 (numerator and denominator share the
-//                 stale max, so the result is exact either way).  Epilogue: O / l ->
-//                 bf16 -> TMA store; lse and attended-key counts per row.
+//   warp 2        Q loader: a unit's query tiles as soon as the previous unit's S
+//                 MMAs have finished reading that shared memory.
+//   softmax WGs   NQT warpgroups; one row per thread (TMEM lane).  Scores are masked
+//                 only on band-edge and global tiles; the running max is kept in the
+//                 log2 domain; P = 2^(x - m) is written back as bf16 over the S
+//                 columns it came from; O is rescaled in TMEM only when a row's max
+//                 grows by more than 2^8 (numerator and denominator share the stale
+//                 max, so the result is exact either way).  Epilogue: O / l -> bf16
+//                 stored straight from registers; lse and attended-key counts.
 // NQT = 2 (head dim <= 128): two query tiles ping-pong -- while one warpgroup turns
 // S_A into P_A the tensor cores run S_B and P_B V -- with TMEM S_A | S_B | O_A | O_B.
 // NQT = 1 (head dim 256): one query tile, S double-buffered, TMEM S0 | S1 | O.
@@ -51,27 +55,27 @@ constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O when the max grows
 
 template <int D>
 struct BandCfg {
-    static constexpr int NQT = D <= 128 ? 2 : 1;     // query tiles per CTA
+    static constexpr int NQT = D <= 128 ? 2 : 1;     // query tiles per unit
     static constexpr int BN = D == 256 ? 64 : 128;  // keys per K/V tile
-    // NQT = 2: warpgroup 0 = producer warp, MMA warp, two idle warps; warpgroups 1, 2 =
-    // softmax.  Twelve warps put three on each SM sub-partition, whose 16K-register
-    // file caps the launch at 168 registers a thread; setmaxnreg then moves registers
-    // from warpgroup 0 (56) to the softmax warpgroups (224):
-    //   128 * 56 + 256 * 224 = 64512 = 384 * 168.
-    // NQT = 1: producer warp, MMA warp and one softmax warpgroup (192 threads).
-    static constexpr int THREADS = NQT == 2 ? 384 : 192;
-    static constexpr int SOFTMAX_WARP0 = NQT == 2 ? 4 : 2;
-    static constexpr int REG_LAUNCH = NQT == 2 ? 168 : 255;
-    static constexpr int REG_CTRL = 56, REG_SOFTMAX = 224;
-    static_assert(NQT == 1 || 128 * REG_CTRL + 256 * REG_SOFTMAX <= THREADS * REG_LAUNCH, "register split");
-    static constexpr int QBYTES = BM * D * 2;        // one query tile (reused for O staging)
-    static constexpr int TBYTES = BN * D * 2;        // one K or V tile
+    // NQT = 2: warpgroup 0 = K/V producer warp, MMA warp, Q loader warp, one idle
+    // warp; warpgroups 1, 2 = softmax.  Twelve warps put three on each SM
+    // sub-partition, whose 16K-register file caps the launch at 168 registers a
+    // thread; setmaxnreg then moves registers from warpgroup 0 (88) to the softmax
+    // warpgroups (208):  128 * 88 + 256 * 208 = 64512 = 384 * 168.
+    // NQT = 1: the same warpgroup 0, then one softmax warpgroup (256 threads).
+    static constexpr int THREADS = NQT == 2 ? 384 : 256;
+    static constexpr int SOFTMAX_WARP0 = 4;
+    static constexpr int REG_CTRL = 88, REG_SOFTMAX = 208;
+    static_assert(NQT == 1 || 128 * REG_CTRL + 256 * REG_SOFTMAX <= THREADS * 168, "register split");
+    static constexpr int QBYTES = BM * D * 2;  // one query tile
+    static constexpr int TBYTES = BN * D * 2;  // one K or V tile
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = NQT * QBYTES;
     static constexpr int NSLOT = (232448 - 2048 - OFF_RING) / TBYTES;
     static constexpr int OFF_BAR = OFF_RING + NSLOT * TBYTES;
-    // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_done[2], pv_done[2], drain
-    static constexpr int NBAR = 1 + 2 * NSLOT + 9;
+    // q_full[2], q_empty[2], kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
+    // o_done[2], o_free[2], pv_done[2], drain
+    static constexpr int NBAR = 2 * NSLOT + 15;
     static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;  // + slack for 1024-B alignment
     static constexpr uint32_t TMEM_COLS = 512;
@@ -83,16 +87,38 @@ struct BandCfg {
 };
 
 struct BandKernelArgs {
-    int B, T, H_q, H_kv, G, TQ, n_units_t;
+    int B, T, H_q, H_kv, G, TQ, n_units_t, n_units;
     int wl, wr;
     float scale_log2;
     const int32_t *global_idx;
     int n_global;
     const __nv_bfloat16 *k, *v;  // for the global-column gather
-    int64_t k_st[3], v_st[3];
+    int64_t k_st[3], v_st[3], o_st[3];
+    __nv_bfloat16 *o;
     float *lse;
     int32_t *counts;
 };
+
+// Geometry of work unit u (units are numbered longest first).
+struct Unit {
+    int b, kvh, t0, kv_lo, n_band, n_tiles;
+};
+
+template <int NQT, int BN>
+__device__ __forceinline__ Unit unit_of(int u, const BandKernelArgs &a) {
+    Unit w;
+    const int bh = u % (a.B * a.H_kv);
+    const int ut = a.n_units_t - 1 - u / (a.B * a.H_kv);
+    w.b = bh / a.H_kv;
+    w.kvh = bh % a.H_kv;
+    w.t0 = ut * NQT * a.TQ;
+    const int t1 = min(a.T - 1, w.t0 + NQT * a.TQ - 1);
+    w.kv_lo = a.wl < 0 ? 0 : max(0, w.t0 - a.wl);
+    const int kv_hi = a.wr < 0 ? a.T - 1 : min(a.T - 1, t1 + a.wr);
+    w.n_band = (kv_hi - w.kv_lo + BN) / BN;
+    w.n_tiles = w.n_band + (a.n_global + BN - 1) / BN;
+    return w;
+}
 
 // Every lane waits (each acquires the barrier); the warp proceeds only if all did,
 // so the .sync.aligned tcgen05 instructions that follow stay convergent.
@@ -104,8 +130,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int D>
 __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     band_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const BandKernelArgs a) {
+                    const __grid_constant__ CUtensorMap tm_v, const BandKernelArgs a) {
     using C = BandCfg<D>;
     constexpr int BN = C::BN, NSLOT = C::NSLOT, NQT = C::NQT;
     extern __shared__ uint8_t smem_raw[];
@@ -118,41 +143,33 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 
     const uint32_t sQ = sbase + C::OFF_Q, sRing = sbase + C::OFF_RING;
     const uint32_t bars = sbase + C::OFF_BAR;
-    auto bar_q = [&]() { return bars; };
-    auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto bar_empty = [&](int s) { return bars + 8u * (1 + NSLOT + s); };
-    auto bar_sf = [&](int i) { return bars + 8u * (1 + 2 * NSLOT + i); };
-    auto bar_pf = [&](int i) { return bars + 8u * (3 + 2 * NSLOT + i); };
-    auto bar_od = [&](int i) { return bars + 8u * (5 + 2 * NSLOT + i); };
-    auto bar_pv = [&](int i) { return bars + 8u * (7 + 2 * NSLOT + i); };
-    const uint32_t bar_drain = bars + 8u * (9 + 2 * NSLOT);
+    auto bar_qf = [&](int x) { return bars + 8u * x; };
+    auto bar_qe = [&](int x) { return bars + 8u * (2 + x); };
+    auto bar_full = [&](int s) { return bars + 8u * (4 + s); };
+    auto bar_empty = [&](int s) { return bars + 8u * (4 + NSLOT + s); };
+    auto bar_sf = [&](int i) { return bars + 8u * (4 + 2 * NSLOT + i); };
+    auto bar_pf = [&](int i) { return bars + 8u * (6 + 2 * NSLOT + i); };
+    auto bar_od = [&](int i) { return bars + 8u * (8 + 2 * NSLOT + i); };
+    auto bar_of = [&](int i) { return bars + 8u * (10 + 2 * NSLOT + i); };
+    auto bar_pv = [&](int i) { return bars + 8u * (12 + 2 * NSLOT + i); };
+    const uint32_t bar_drain = bars + 8u * (14 + 2 * NSLOT);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
 
-    // ---- unit decode (longest units first: query-tile groups in decreasing order)
-    const int bh = blockIdx.x % (a.B * a.H_kv);
-    const int ut = a.n_units_t - 1 - blockIdx.x / (a.B * a.H_kv);
-    const int b = bh / a.H_kv, kvh = bh % a.H_kv;
-    const int t0 = ut * NQT * a.TQ;
-    const int t1 = min(a.T - 1, t0 + NQT * a.TQ - 1);
-    const int kv_lo = a.wl < 0 ? 0 : max(0, t0 - a.wl);
-    const int kv_hi = a.wr < 0 ? a.T - 1 : min(a.T - 1, t1 + a.wr);
-    const int n_band = (kv_hi - kv_lo + BN) / BN;
-    const int n_gt = (a.n_global + BN - 1) / BN;
-    const int n_tiles = n_band + n_gt;
-
-    // ---- setup: barriers, TMEM
+    // ---- setup: barriers, TMEM (once per CTA)
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bar_q(), 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar_qf(x), 1);
+            mbar_init(bar_qe(x), 4);  // the four warps of the tile's softmax warpgroup
+            mbar_init(bar_sf(x), 1);
+            mbar_init(bar_pf(x), 4);
+            mbar_init(bar_od(x), 1);
+            mbar_init(bar_of(x), 4);
+            mbar_init(bar_pv(x), 1);
+        }
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(bar_full(s), 1);
             mbar_init(bar_empty(s), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_sf(i), 1);
-            mbar_init(bar_pf(i), 4);
-            mbar_init(bar_od(i), 1);
-            mbar_init(bar_pv(i), 1);
         }
         mbar_init(bar_drain, 1);
         fence_mbar_init();
@@ -165,7 +182,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -174,74 +190,97 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     volatile int *abort = &abort_flag;
 
     if (warp == 0) {
-        // ============================ producer ============================
+        // ============================ K/V producer ============================
         if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
-        int n_issued = 0;  // ring fills issued so far
-        if (lane == 0) {
-            uint32_t qbytes = 0;
-#pragma unroll
-            for (int x = 0; x < NQT; ++x)
-                if (t0 + x * a.TQ < a.T) qbytes += static_cast<uint32_t>(a.G * a.TQ * D * 2);
-            mbar_arrive_expect_tx(bar_q(), qbytes);
-#pragma unroll
-            for (int x = 0; x < NQT; ++x) {
-                if (t0 + x * a.TQ >= a.T) continue;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sQ + x * C::QBYTES + c * (BM * 128), &tm_q, bar_q(), c * 64, kvh * a.G,
-                                t0 + x * a.TQ, b);
-            }
-        }
+        int g = 0;  // ring fills issued so far (all units)
         bool ok = true;
 #pragma unroll 1
-        for (int i = 0; i < 2 * n_tiles; ++i) {
-            const int s = i % NSLOT;
-            if (i >= NSLOT) ok = warp_wait(bar_empty(s), ((i / NSLOT) - 1) & 1, abort);
-            if (!ok) break;
-            const int j = i >> 1;
-            const bool is_v = (i & 1) != 0;
-            const uint32_t dst = sRing + s * C::TBYTES;
-            if (j < n_band) {
-                if (lane == 0) {
-                    const int k0 = kv_lo + j * BN;
-                    mbar_arrive_expect_tx(bar_full(s), C::TBYTES);
+        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+            const Unit w = unit_of<NQT, BN>(u, a);
+#pragma unroll 1
+            for (int i = 0; i < 2 * w.n_tiles; ++i) {
+                const int s = g % NSLOT;
+                if (g >= NSLOT) ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
+                if (!ok) break;
+                const int j = i >> 1;
+                const bool is_v = (i & 1) != 0;
+                const uint32_t dst = sRing + s * C::TBYTES;
+                if (j < w.n_band) {
+                    if (lane == 0) {
+                        const int k0 = w.kv_lo + j * BN;
+                        mbar_arrive_expect_tx(bar_full(s), C::TBYTES);
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_4d(dst + c * (BN * 128), is_v ? &tm_v : &tm_k, bar_full(s), c * 64, kvh, k0, b);
-                }
-            } else {
-                // global-column tile: rows global_idx[g0 + r] (zero rows past the list)
-                const int g0 = (j - n_band) * BN;
-                const __nv_bfloat16 *src = is_v ? a.v : a.k;
-                const int64_t *st = is_v ? a.v_st : a.k_st;
-                constexpr int kPieces = D / 8;
-                for (int idx = lane; idx < BN * kPieces; idx += 32) {
-                    const int r = idx / kPieces, pc = idx % kPieces;
-                    const int gi = g0 + r;
-                    int srow = -1;
-                    if (gi < a.n_global) {
-                        const int gs = a.global_idx[gi];
-                        if (gs >= 0 && gs < a.T) srow = gs;
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d(dst + c * (BN * 128), is_v ? &tm_v : &tm_k, bar_full(s), c * 64, w.kvh, k0,
+                                        w.b);
                     }
-                    uint4 val = make_uint4(0, 0, 0, 0);
-                    if (srow >= 0)
-                        val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(b) * st[0] +
-                                                               static_cast<int64_t>(srow) * st[1] +
-                                                               static_cast<int64_t>(kvh) * st[2] + pc * 8);
-                    const uint32_t off = (pc >> 3) * (BN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sgen + C::OFF_RING + s * C::TBYTES + off) = val;
+                } else {
+                    // global-column tile: rows global_idx[g0 + r] (zero rows past the list)
+                    const int g0 = (j - w.n_band) * BN;
+                    const __nv_bfloat16 *src = is_v ? a.v : a.k;
+                    const int64_t *st = is_v ? a.v_st : a.k_st;
+                    constexpr int kPieces = D / 8;
+                    for (int idx = lane; idx < BN * kPieces; idx += 32) {
+                        const int r = idx / kPieces, pc = idx % kPieces;
+                        const int gi = g0 + r;
+                        int srow = -1;
+                        if (gi < a.n_global) {
+                            const int gs = a.global_idx[gi];
+                            if (gs >= 0 && gs < a.T) srow = gs;
+                        }
+                        uint4 val = make_uint4(0, 0, 0, 0);
+                        if (srow >= 0)
+                            val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(w.b) * st[0] +
+                                                                   static_cast<int64_t>(srow) * st[1] +
+                                                                   static_cast<int64_t>(w.kvh) * st[2] + pc * 8);
+                        const uint32_t off = (pc >> 3) * (BN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(sgen + C::OFF_RING + s * C::TBYTES + off) = val;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_full(s));
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_full(s));
+                ++g;
             }
-            n_issued = i + 1;
         }
         if (!ok && lane == 0) {
             // drain the copies still in flight (at most the last NSLOT fills) before exit
-            mbar_drain(bar_q(), 0, &g_band_err);
-            for (int i = max(0, n_issued - NSLOT); i < n_issued; ++i)
-                if ((i >> 1) < n_band) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err);
+            for (int i = max(0, g - NSLOT); i < g; ++i) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err);
+        }
+    } else if (warp == 2) {
+        // ============================ Q loader ============================
+        if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
+        int k = 0;
+        int issued[2] = {0, 0};  // query loads issued per tile
+        bool ok = true;
+#pragma unroll 1
+        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+            const Unit w = unit_of<NQT, BN>(u, a);
+#pragma unroll 1
+            for (int x = 0; x < NQT && ok; ++x) {
+                // the previous unit's S MMAs are done with this tile's shared memory
+                if (k >= 1) ok = warp_wait(bar_qe(x), (k - 1) & 1, abort);
+                if (!ok) break;
+                if (lane == 0) {
+                    const int tx = w.t0 + x * a.TQ;
+                    if (tx < a.T) {
+                        mbar_arrive_expect_tx(bar_qf(x), static_cast<uint32_t>(a.G * a.TQ * D * 2));
+#pragma unroll
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d(sQ + x * C::QBYTES + c * (BM * 128), &tm_q, bar_qf(x), c * 64, w.kvh * a.G,
+                                        tx, w.b);
+                    } else {
+                        mbar_arrive(bar_qf(x));  // tile past the sequence end: nothing to load
+                    }
+                }
+                __syncwarp();
+                ++issued[x];
+            }
+        }
+        if (!ok && lane == 0) {
+            // drain the last query copy of each tile before exit
+            for (int x = 0; x < NQT; ++x)
+                if (issued[x] > 0) mbar_drain(bar_qf(x), (issued[x] - 1) & 1, &g_band_err);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
@@ -249,10 +288,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(BM, D, false, true);
-            bool ok = mbar_wait(bar_q(), 0, abort, &g_band_err);
-            // S into TMEM slot `slot` from query tile `qt` and the K tile of key tile j.
-            auto mma_s = [&](int slot, int qt, int j, bool wait_k) -> bool {
-                const int fi = 2 * j, s = fi % NSLOT;
+            bool ok = true;
+            int J = 0;  // key tiles of this CTA's previous units
+            int k = 0;  // units of this CTA so far
+            // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
+            auto mma_s = [&](int slot, int qt, int jg, bool wait_k) -> bool {
+                const int fi = 2 * jg, s = fi % NSLOT;
                 if (wait_k && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
@@ -264,77 +305,90 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 }
                 return true;
             };
-            // O_tile += P(slot) V_j
-            auto mma_pv = [&](int slot, int otile, int j, int p_parity, bool wait_v) -> bool {
-                const int fi = 2 * j + 1, s = fi % NSLOT;
+            // O_tile (+)= P(slot) V of global tile index jg; `first` starts a fresh O.
+            auto mma_pv = [&](int slot, int otile, int jg, uint32_t p_parity, bool wait_v, bool first) -> bool {
+                const int fi = 2 * jg + 1, s = fi % NSLOT;
                 if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
                 if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
+                // the previous unit's epilogue has read this O accumulator out
+                if (first && k >= 1 && !mbar_wait(bar_of(otile), (k - 1) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t vb = sRing + s * C::TBYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bd = smem_desc(vb + kk * 2048, BN * 128, 1024, kSwizzle128B);
                     tc_mma_ts(tmem + C::tm_o(otile), tmem + C::tm_s(slot) + kk * 8, bd, idPV,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                              (!first || kk > 0) ? 1u : 0u);
                 }
                 return true;
             };
-            auto kslot = [&](int j) { return (2 * j) % NSLOT; };
-            auto vslot = [&](int j) { return (2 * j + 1) % NSLOT; };
-            if constexpr (NQT == 2) {
-                if (ok) ok = mma_s(0, 0, 0, true);
-                if (ok) {
-                    tc_commit(bar_sf(0));
-                    ok = mma_s(1, 1, 0, false);
-                }
-                if (ok) {
-                    tc_commit(bar_sf(1));
-                    tc_commit(bar_empty(kslot(0)));
-                }
+            auto kslot = [&](int jg) { return (2 * jg) % NSLOT; };
+            auto vslot = [&](int jg) { return (2 * jg + 1) % NSLOT; };
 #pragma unroll 1
-                for (int j = 0; j < n_tiles && ok; ++j) {
-                    ok = mma_pv(0, 0, j, j & 1, true);
-                    if (!ok) break;
-                    if (j + 1 < n_tiles) {
-                        ok = mma_s(0, 0, j + 1, true);
-                        if (!ok) break;
+            for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+                const int n = unit_of<NQT, BN>(u, a).n_tiles;
+                // each query tile is waited for just before its first S MMA
+                ok = mbar_wait(bar_qf(0), k & 1, abort, &g_band_err);
+                if (!ok) break;
+                if constexpr (NQT == 2) {
+                    ok = mma_s(0, 0, J, true);
+                    if (ok) {
                         tc_commit(bar_sf(0));
-                    } else {
-                        tc_commit(bar_od(0));
+                        ok = mbar_wait(bar_qf(1), k & 1, abort, &g_band_err);
                     }
-                    ok = mma_pv(1, 1, j, j & 1, false);
-                    if (!ok) break;
-                    tc_commit(bar_empty(vslot(j)));
-                    if (j + 1 < n_tiles) {
-                        ok = mma_s(1, 1, j + 1, false);
-                        if (!ok) break;
+                    if (ok) ok = mma_s(1, 1, J, false);
+                    if (ok) {
                         tc_commit(bar_sf(1));
-                        tc_commit(bar_empty(kslot(j + 1)));
-                    } else {
-                        tc_commit(bar_od(1));
+                        tc_commit(bar_empty(kslot(J)));
                     }
-                }
-            } else {
-                if (ok) ok = mma_s(0, 0, 0, true);
-                if (ok) {
-                    tc_commit(bar_sf(0));
-                    tc_commit(bar_empty(kslot(0)));
-                }
 #pragma unroll 1
-                for (int j = 0; j < n_tiles && ok; ++j) {
-                    if (j + 1 < n_tiles) {
-                        // slot (j+1)&1 last held P_{j-1}, consumed by PV_{j-1} issued earlier
-                        ok = mma_s((j + 1) & 1, 0, j + 1, true);
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int jg = J + j;
+                        ok = mma_pv(0, 0, jg, jg & 1, true, j == 0);
                         if (!ok) break;
-                        tc_commit(bar_sf((j + 1) & 1));
-                        tc_commit(bar_empty(kslot(j + 1)));
+                        if (j + 1 < n) {
+                            ok = mma_s(0, 0, jg + 1, true);
+                            if (!ok) break;
+                            tc_commit(bar_sf(0));
+                        } else {
+                            tc_commit(bar_od(0));
+                        }
+                        ok = mma_pv(1, 1, jg, jg & 1, false, j == 0);
+                        if (!ok) break;
+                        tc_commit(bar_empty(vslot(jg)));
+                        if (j + 1 < n) {
+                            ok = mma_s(1, 1, jg + 1, false);
+                            if (!ok) break;
+                            tc_commit(bar_sf(1));
+                            tc_commit(bar_empty(kslot(jg + 1)));
+                        } else {
+                            tc_commit(bar_od(1));
+                        }
                     }
-                    ok = mma_pv(j & 1, 0, j, (j >> 1) & 1, true);
-                    if (!ok) break;
-                    tc_commit(bar_pv(j & 1));
-                    tc_commit(bar_empty(vslot(j)));
-                    if (j + 1 == n_tiles) tc_commit(bar_od(0));
+                } else {
+                    ok = mma_s(J & 1, 0, J, true);
+                    if (ok) {
+                        tc_commit(bar_sf(J & 1));
+                        tc_commit(bar_empty(kslot(J)));
+                    }
+#pragma unroll 1
+                    for (int j = 0; j < n && ok; ++j) {
+                        const int jg = J + j;
+                        if (j + 1 < n) {
+                            // slot (jg+1)&1 last held P of tile jg-1, consumed by its P V issued earlier
+                            ok = mma_s((jg + 1) & 1, 0, jg + 1, true);
+                            if (!ok) break;
+                            tc_commit(bar_sf((jg + 1) & 1));
+                            tc_commit(bar_empty(kslot(jg + 1)));
+                        }
+                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0);
+                        if (!ok) break;
+                        tc_commit(bar_pv(jg & 1));
+                        tc_commit(bar_empty(vslot(jg)));
+                        if (j + 1 == n) tc_commit(bar_od(0));
+                    }
                 }
+                J += n;
             }
             if (!ok) {
                 tc_commit(bar_drain);
@@ -348,177 +402,183 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         const int wg = (warp - C::SOFTMAX_WARP0) >> 2;  // query tile of this warpgroup
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // row == TMEM lane
-        const int tx = t0 + wg * a.TQ;      // first token of this warpgroup's query tile
         const int tq = r / a.G, hj = r % a.G;
-        const int t = tx + tq;
-        const bool row_ok = tq < a.TQ && t < a.T;
-        const int h = kvh * a.G + hj;
-        const int tlo = tx, thi = min(a.T - 1, tx + a.TQ - 1);
-        // this row's band, clipped to [0, T)
-        const int lo_abs = a.wl < 0 ? 0 : max(0, t - a.wl);
-        const int hi_abs = a.wr < 0 ? a.T - 1 : min(a.T - 1, t + a.wr);
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t o_addr = tmem + lane_addr + C::tm_o(wg);
-        float m = -INFINITY, l = 0.f;
-        int count = 0;
         bool ok = true;
+        int J = 0, k = 0;
 #pragma unroll 1
-        for (int j = 0; j < n_tiles; ++j) {
-            const int slot = NQT == 2 ? wg : (j & 1);
-            const uint32_t parity = NQT == 2 ? (j & 1) : ((j >> 1) & 1);
-            if (!warp_wait(bar_sf(slot), parity, abort)) {
+        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+            const Unit w = unit_of<NQT, BN>(u, a);
+            const int tx = w.t0 + wg * a.TQ;  // first token of this warpgroup's query tile
+            const int t = tx + tq;
+            const bool row_ok = tq < a.TQ && t < a.T;
+            const int h = w.kvh * a.G + hj;
+            const int tlo = tx, thi = min(a.T - 1, tx + a.TQ - 1);
+            // this row's band, clipped to [0, T)
+            const int lo_abs = a.wl < 0 ? 0 : max(0, t - a.wl);
+            const int hi_abs = a.wr < 0 ? a.T - 1 : min(a.T - 1, t + a.wr);
+            float m = -INFINITY, l = 0.f;
+            int count = 0;
+#pragma unroll 1
+            for (int j = 0; j < w.n_tiles; ++j) {
+                const int jg = J + j;
+                const int slot = NQT == 2 ? wg : (jg & 1);
+                const uint32_t parity = NQT == 2 ? (jg & 1) : ((jg >> 1) & 1);
+                if (!warp_wait(bar_sf(slot), parity, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s_addr = tmem + lane_addr + C::tm_s(slot);
+                float x[BN];
+                {
+                    uint32_t raw[BN / 32][32];
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, raw[c]);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
+                }
+                // ---- mask (branch-free; only band-edge and global tiles)
+                if (j < w.n_band) {
+                    const int k0 = w.kv_lo + j * BN;
+                    const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
+                                          (k0 + BN - 1 <= a.T - 1);
+                    if (interior) {
+                        count += BN;
+                    } else {
+                        // allowed columns of this row form one run [lo, lo + len)
+                        const int lo = min(max(lo_abs - k0, 0), BN);
+                        const int hi = min(max(hi_abs - k0 + 1, 0), BN);
+                        const int len = max(hi - lo, 0);
+                        count += len;
+#pragma unroll
+                        for (int c = 0; c < BN; ++c)
+                            x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
+                    }
+                } else {
+                    // global columns: each lane loads BN/32 of this tile's positions, shuffles
+                    // broadcast them; keep the ones outside the row's band
+                    const int g0 = (j - w.n_band) * BN;
+                    int gv[BN / 32];
+#pragma unroll
+                    for (int i = 0; i < BN / 32; ++i) {
+                        const int gi = g0 + i * 32 + lane;
+                        gv[i] = gi < a.n_global ? __ldg(a.global_idx + gi) : -1;
+                    }
+                    int cnt4[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) {
+                        const int gs = __shfl_sync(0xffffffffu, gv[c >> 5], c & 31);
+                        const bool al = (gs >= 0) & (gs < a.T) & ((gs < lo_abs) | (gs > hi_abs));
+                        cnt4[c & 3] += al ? 1 : 0;
+                        x[c] = al ? x[c] : -INFINITY;
+                    }
+                    count += (cnt4[0] + cnt4[1]) + (cnt4[2] + cnt4[3]);
+                }
+                // ---- running max (log2 domain), tree reduction
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                for (int c = 8; c < BN; c += 8)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[c + i]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float mt = mx * a.scale_log2;
+                const bool need = mt > m + kRescaleTau;
+                const float mu = need ? mt : m;
+                const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
+                if (__any_sync(0xffffffffu, need) && j > 0) {
+                    // O holds P V of tiles 0 .. j-1 of this unit and must be complete.
+                    if constexpr (NQT == 1) {
+                        if (!warp_wait(bar_pv((jg - 1) & 1), ((jg - 1) >> 1) & 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_addr + c * 32, ov);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(o_addr + c * 32, ov);
+                    }
+                }
+                m = mu;
+                const float msub = mu == -INFINITY ? 0.f : mu;
+                // ---- P = 2^(x*scale_log2 - m) as bf16 pairs over the first BN/2 S columns
+                float rs8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+                for (int hlf = 0; hlf < BN / 64; ++hlf) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ex2(fmaf(x[hlf * 64 + 2 * e], a.scale_log2, -msub));
+                        const float p1 = ex2(fmaf(x[hlf * 64 + 2 * e + 1], a.scale_log2, -msub));
+                        rs8[e & 7] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_addr + hlf * 32, pk);
+                }
+                tc_wait_st();
+                l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_pf(slot));
+            }
+            if (!ok) break;
+
+            // ---- epilogue: O is final once this tile's last P V completes
+            if (!warp_wait(bar_od(wg), k & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_addr = tmem + lane_addr + C::tm_s(slot);
-            float x[BN];
-            {
-                uint32_t raw[BN / 32][32];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, raw[c]);
-                tc_wait_ld();
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
-            }
-            // ---- mask (branch-free; only band-edge and global tiles)
-            if (j < n_band) {
-                const int k0 = kv_lo + j * BN;
-                const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
-                                      (k0 + BN - 1 <= a.T - 1);
-                if (interior) {
-                    count += BN;
-                } else {
-                    // allowed columns of this row form one run [lo, lo + len)
-                    const int lo = min(max(lo_abs - k0, 0), BN);
-                    const int hi = min(max(hi_abs - k0 + 1, 0), BN);
-                    const int len = max(hi - lo, 0);
-                    count += len;
-#pragma unroll
-                    for (int c = 0; c < BN; ++c)
-                        x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
-                }
-            } else {
-                // global columns: each lane loads BN/32 of this tile's positions, shuffles
-                // broadcast them; keep the ones outside the row's band
-                const int g0 = (j - n_band) * BN;
-                int gv[BN / 32];
-#pragma unroll
-                for (int i = 0; i < BN / 32; ++i) {
-                    const int gi = g0 + i * 32 + lane;
-                    gv[i] = gi < a.n_global ? __ldg(a.global_idx + gi) : -1;
-                }
-                int cnt4[4] = {0, 0, 0, 0};
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const int gs = __shfl_sync(0xffffffffu, gv[c >> 5], c & 31);
-                    const bool al = (gs >= 0) & (gs < a.T) & ((gs < lo_abs) | (gs > hi_abs));
-                    cnt4[c & 3] += al ? 1 : 0;
-                    x[c] = al ? x[c] : -INFINITY;
-                }
-                count += (cnt4[0] + cnt4[1]) + (cnt4[2] + cnt4[3]);
-            }
-            // ---- running max (log2 domain), tree reduction
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = x[i];
-#pragma unroll
-            for (int c = 8; c < BN; c += 8)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[c + i]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float mt = mx * a.scale_log2;
-            const bool need = mt > m + kRescaleTau;
-            const float mu = need ? mt : m;
-            const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
-            if (__any_sync(0xffffffffu, need) && j > 0) {
-                // O holds P V of tiles 0 .. j-1 and must be complete before it is rescaled.
-                if constexpr (NQT == 1) {
-                    if (!warp_wait(bar_pv((j - 1) & 1), ((j - 1) >> 1) & 1, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(o_addr + c * 32, ov);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(o_addr + c * 32, ov);
-                }
-            }
-            m = mu;
-            const float msub = mu == -INFINITY ? 0.f : mu;
-            // ---- P = 2^(x*scale_log2 - m) as bf16 pairs over the first BN/2 S columns
-            float rs8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll
-            for (int hlf = 0; hlf < BN / 64; ++hlf) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2(fmaf(x[hlf * 64 + 2 * e], a.scale_log2, -msub));
-                    const float p1 = ex2(fmaf(x[hlf * 64 + 2 * e + 1], a.scale_log2, -msub));
-                    rs8[e & 7] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(s_addr + hlf * 32, pk);
-            }
-            tc_wait_st();
-            l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pf(slot));
-        }
-
-        // ---- epilogue
-        if (ok) ok = warp_wait(bar_od(wg), 0, abort);
-        const bool all_ok = ok && *abort == 0;
-        const uint32_t stage = sQ + wg * C::QBYTES;  // this tile's Q region, free once O is final
-        if (all_ok) {
-            tc_fence_after();
+            // every MMA of this unit has completed: the Q loader may refill this tile
+            if (lane == 0) mbar_arrive(bar_qe(wg));
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = a.o + static_cast<int64_t>(w.b) * a.o_st[0] + static_cast<int64_t>(t) * a.o_st[1] +
+                                  static_cast<int64_t>(h) * a.o_st[2];
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(o_addr + c * 32, ov);
                 tc_wait_ld();
+                if (row_ok) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t w[4];
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t wv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 2 * e]) * inv_l,
-                                           __uint_as_float(ov[q4 * 8 + 2 * e + 1]) * inv_l);
-                    const int pc = c * 4 + q4;  // 16-byte piece index along d
-                    const uint32_t off = (pc >> 3) * (BM * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sgen + C::OFF_Q + wg * C::QBYTES + off) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int e = 0; e < 4; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 2 * e]) * inv_l,
+                                                __uint_as_float(ov[q4 * 8 + 2 * e + 1]) * inv_l);
+                        *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
                 }
             }
-            fence_proxy_async_smem();
+            // O has been read out: the next unit's first P V may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_of(wg));
             if (row_ok) {
-                const int64_t li = (static_cast<int64_t>(b) * a.H_q + h) * a.T + t;
+                const int64_t li = (static_cast<int64_t>(w.b) * a.H_q + h) * a.T + t;
                 a.lse[li] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 if (a.counts) a.counts[li] = count;
             }
-        }
-        // the warpgroup's rows are staged before one of its threads issues the store
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
-        if (all_ok && ((warp - C::SOFTMAX_WARP0) & 3) == 0 && lane == 0 && tx < a.T) {
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) tma_store_4d(&tm_o, stage + c * (BM * 128), c * 64, kvh * a.G, tx, b);
-            tma_store_commit();
-            tma_store_wait_all();
+            J += w.n_tiles;
         }
     } else {
-        // idle warps of warpgroup 0 give their registers to the softmax warpgroups
+        // idle warp of warpgroup 0 gives its registers to the softmax warpgroups
         if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
     }
 
@@ -561,6 +621,18 @@ bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int B, cons
     return r == CUDA_SUCCESS;
 }
 
+int band_sm_count() {
+    static int n[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!n[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
 template <int D>
 cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     using C = BandCfg<D>;
@@ -572,11 +644,10 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     }
     const int G = x.H_q / x.H_kv;
     const int TQ = BM / G;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, x.q, D, x.H_q, x.T, x.B, x.q_st, G, TQ) ||
         !make_map(&mk, x.k, D, x.H_kv, x.T, x.B, x.k_st, 1, C::BN) ||
-        !make_map(&mv, x.v, D, x.H_kv, x.T, x.B, x.v_st, 1, C::BN) ||
-        !make_map(&mo, x.o, D, x.H_q, x.T, x.B, x.o_st, G, TQ))
+        !make_map(&mv, x.v, D, x.H_kv, x.T, x.B, x.v_st, 1, C::BN))
         return cudaErrorInvalidValue;
     BandKernelArgs a{};
     a.B = x.B;
@@ -597,12 +668,16 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     for (int i = 0; i < 3; ++i) {
         a.k_st[i] = x.k_st[i];
         a.v_st[i] = x.v_st[i];
+        a.o_st[i] = x.o_st[i];
     }
+    a.o = static_cast<__nv_bfloat16 *>(x.o);
     a.lse = x.lse;
     a.counts = x.counts;
     const long long units = static_cast<long long>(x.B) * x.H_kv * a.n_units_t;
     if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    band_fwd_kernel<D><<<static_cast<unsigned>(units), C::THREADS, C::SMEM, s>>>(mq, mk, mv, mo, a);
+    a.n_units = static_cast<int>(units);
+    const int grid = static_cast<int>(units < band_sm_count() ? units : band_sm_count());
+    band_fwd_kernel<D><<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 

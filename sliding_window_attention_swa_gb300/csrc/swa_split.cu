@@ -187,7 +187,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 if (!emit) continue;
                 const int st = seq % NST;
                 if (seq >= NST) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
+                    ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
                     if (!ok) break;
                 }
                 if (lane == 0) {
@@ -232,7 +232,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 #pragma unroll 1
         for (int seq = 0; ok; ++seq) {
             const int st = seq % NST;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_full(st), (seq / NST) & 1, abort, &g_split_err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_full(st), (seq / NST) & 1, abort, &g_split_err))) {
                 ok = false;
                 break;
             }
@@ -372,7 +372,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                     ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
                     ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
                 }
-                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_cd, (n_done - 1) & 1, abort, &g_split_err))) {
+                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_cd, (n_done - 1) & 1, abort, &g_split_err))) {
                     ok = false;
                     break;
                 }
@@ -396,7 +396,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_cf);
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_cf, n_done & 1, abort, &g_split_err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_cf, n_done & 1, abort, &g_split_err))) {
                     ok = false;
                     break;
                 }
