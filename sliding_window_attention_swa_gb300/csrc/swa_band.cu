@@ -479,16 +479,20 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     }
                     count += (cnt4[0] + cnt4[1]) + (cnt4[2] + cnt4[3]);
                 }
-                // ---- running max (log2 domain), tree reduction
+                // ---- running max (log2 domain): eight chains of three-input maxima
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = x[i];
 #pragma unroll
-                for (int c = 8; c < BN; c += 8)
+                for (int c = 8; c + 8 < BN; c += 16)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[c + i]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], x[c + i], x[c + 8 + i]);
+                if constexpr ((BN / 8) % 2 == 0) {  // one column block of 8 left over
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], x[BN - 8 + i]);
+                }
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float mt = mx * a.scale_log2;
                 const bool need = mt > m + kRescaleTau;
                 const float mu = need ? mt : m;
@@ -514,24 +518,34 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 }
                 m = mu;
                 const float msub = mu == -INFINITY ? 0.f : mu;
-                // ---- P = 2^(x*scale_log2 - m) as bf16 pairs over the first BN/2 S columns
-                float rs8[8];
+                // ---- P = 2^(x*scale_log2 - m) as bf16 pairs over the first BN/2 S columns;
+                // the scale-and-shift and the row sum run on column pairs (fp32x2)
+                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-msub, -msub);
+                uint64_t rs2[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+                for (int i = 0; i < 4; ++i) rs2[i] = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int hlf = 0; hlf < BN / 64; ++hlf) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ex2(fmaf(x[hlf * 64 + 2 * e], a.scale_log2, -msub));
-                        const float p1 = ex2(fmaf(x[hlf * 64 + 2 * e + 1], a.scale_log2, -msub));
-                        rs8[e & 7] += p0 + p1;
+                        float t0, t1;
+                        f2_unpack(f2_fma(f2_pack(x[hlf * 64 + 2 * e], x[hlf * 64 + 2 * e + 1]), sc2, nm2), t0, t1);
+                        const float p0 = ex2(t0), p1 = ex2(t1);
+                        rs2[e & 3] = f2_add(rs2[e & 3], f2_pack(p0, p1));
                         pk[e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(s_addr + hlf * 32, pk);
                 }
                 tc_wait_st();
-                l = l * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                float rsum;
+                {
+                    const uint64_t r01 = f2_add(rs2[0], rs2[1]), r23 = f2_add(rs2[2], rs2[3]);
+                    float lo, hi;
+                    f2_unpack(f2_add(r01, r23), lo, hi);
+                    rsum = lo + hi;
+                }
+                l = l * alpha + rsum;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_pf(slot));
