@@ -8,7 +8,7 @@
 // prathamp.com "Sliding Window Attention: From Local Windows to Global Context",
 // section 4.3).  The work is HBM-bound: every valid key/value byte is read once.
 //
-// Persistent kernel, one CTA per SM, five warps:
+// Persistent kernel, two CTAs per SM for head dim <= 128 (one for 256), five warps:
 //   warp 0     producer.  Walks this CTA's work items (batch, kv head, query block,
 //              512-slot split) in a static round-robin order.  For each item it
 //              reads the slot positions, builds one 64-bit validity mask per
