@@ -308,6 +308,252 @@ def check_workload_counts(lib):
         assert int(oracle.mask_row(T, T - 1, W - 1, 0, lib=lib).sum()) == W
 
 
+# ----------------------------------------------------------------------------- dilation
+def check_dilated_n16_rows(lib):
+    meta, rows, total, _ = _read_rows("longformer_n16_r2_d2_dilated_rows.txt")
+    n, r, d = meta["n"][0], meta["r"][0], meta["d"][0]
+    got_total = 0
+    for t in range(n):
+        m = oracle.mask_row(n, t, r, r, lib=lib, dil=d)
+        keys, cnt = rows[t]
+        assert list(np.nonzero(m)[0]) == keys, (t, np.nonzero(m)[0], keys)
+        assert int(m.sum()) == cnt
+        got_total += cnt
+    assert got_total == total == 68
+
+
+def check_dilated_closed_forms(lib):
+    # Causal dilated window {t - i*d : 0 <= i < W} (lizeman page, "Dilation"):
+    # min(W, floor(t/d) + 1) keys.  Symmetric dilated band: the undilated count of
+    # the row's residue class, i.e. min(r, floor(t/d)) + min(r, floor((n-1-t)/d)) + 1.
+    for T, W, d in [(50, 4, 3), (40, 7, 2), (33, 1, 5), (64, 8, 8)]:
+        for t in range(T):
+            m = oracle.mask_row(T, t, W - 1, 0, lib=lib, dil=d)
+            assert int(m.sum()) == min(W, t // d + 1), (T, W, d, t)
+            assert all((t - s) % d == 0 and 0 <= t - s < W * d for s in np.nonzero(m)[0])
+    for n, r, d in [(16, 2, 2), (45, 3, 4), (30, 6, 3)]:
+        for t in range(n):
+            want = min(r, t // d) + min(r, (n - 1 - t) // d) + 1
+            assert int(oracle.mask_row(n, t, r, r, lib=lib, dil=d).sum()) == want
+
+
+def check_dilated_residue_identity(lib):
+    # Dilation d splits the sequence into d residue classes; on each class the
+    # dilated band is the ordinary band of the subsequence (same wl, wr in steps).
+    q, k, v = _rand_case(70, 2, 37, 4, 2, 16)
+    dil = [1, 2, 3, 2]
+    o, lse, cnt = oracle.fwd(q, k, v, 3, 2, 0.2, lib=lib, dilation=dil)
+    for h, d in enumerate(dil):
+        for r in range(d):
+            o2, lse2, cnt2 = oracle.fwd(q[:, r::d], k[:, r::d], v[:, r::d], 3, 2, 0.2, lib=lib)
+            np.testing.assert_array_equal(o[:, h, r::d], o2[:, h])
+            np.testing.assert_array_equal(lse[:, h, r::d], lse2[:, h])
+            np.testing.assert_array_equal(cnt[:, h, r::d], cnt2[:, h])
+
+
+def check_dilated_bruteforce(lib):
+    cases = [
+        (1, 16, 2, 1, 16, 2, 2, [2, 1]),
+        (1, 30, 4, 2, 8, 3, 0, [1, 2, 3, 4]),
+        (2, 25, 2, 2, 16, -1, 1, [3, 2]),
+    ]
+    for i, (B, T, Hq, Hkv, D, wl, wr, dil) in enumerate(cases):
+        q, k, v = _rand_case(80 + i, B, T, Hq, Hkv, D)
+        o, lse, cnt = oracle.fwd(q, k, v, wl, wr, 0.3, lib=lib, dilation=dil)
+        ob, lseb, cntb = oracle.dense_bruteforce(q, k, v, wl, wr, 0.3, dilation=dil)
+        np.testing.assert_allclose(o, ob, atol=1e-12, rtol=1e-10)
+        np.testing.assert_allclose(lse, lseb, atol=1e-12, rtol=1e-10)
+        np.testing.assert_array_equal(cnt, cntb)
+
+
+# ----------------------------------------------------------------------------- sinks
+def check_sink_counts(lib):
+    # Causal window W plus sinks {0..ns-1}: the band's min(t+1, W) keys plus the
+    # sinks left of it, max(0, min(ns, t-W+1)).  Bidirectional radius r: sinks are
+    # kept only left of the band (a sink right of it is beyond t + r).
+    S = oracle.GLOBAL_SINK
+    for T, W, ns in [(40, 4, 3), (64, 16, 4), (20, 25, 2), (30, 1, 1)]:
+        for t in range(T):
+            m = oracle.mask_row(T, t, W - 1, 0, list(range(ns)), lib=lib, gmode=S)
+            assert int(m.sum()) == min(t + 1, W) + max(0, min(ns, t - W + 1)), (T, W, ns, t)
+            assert not m[t + 1:].any()
+    for n, r, ns in [(30, 3, 4), (16, 2, 2)]:
+        for t in range(n):
+            m = oracle.mask_row(n, t, r, r, list(range(ns)), lib=lib, gmode=S)
+            band = min(n - 1, t + r) - max(0, t - r) + 1
+            assert int(m.sum()) == band + max(0, min(ns, t - r)), (n, r, ns, t)
+
+
+def check_sink_bruteforce(lib):
+    S = oracle.GLOBAL_SINK
+    cases = [
+        (1, 40, 2, 1, 16, 5, 0, [0, 1, 2, 3]),
+        (2, 33, 4, 2, 16, 3, 2, [0, 5, 17]),
+        (1, 24, 2, 2, 8, -1, 0, [0]),
+    ]
+    for i, (B, T, Hq, Hkv, D, wl, wr, G) in enumerate(cases):
+        q, k, v = _rand_case(90 + i, B, T, Hq, Hkv, D)
+        o, lse, cnt = oracle.fwd(q, k, v, wl, wr, 0.25, G, lib=lib, gmode=S)
+        ob, lseb, cntb = oracle.dense_bruteforce(q, k, v, wl, wr, 0.25, G, gmode=S)
+        np.testing.assert_allclose(o, ob, atol=1e-12, rtol=1e-10)
+        np.testing.assert_allclose(lse, lseb, atol=1e-12, rtol=1e-10)
+        np.testing.assert_array_equal(cnt, cntb)
+    # Sinks already inside every row's band change nothing (window >= T).
+    q, k, v = _rand_case(95, 1, 20, 2, 1, 16)
+    o, lse, cnt = oracle.fwd(q, k, v, 19, 0, 0.25, [0, 1], lib=lib, gmode=S)
+    o2, lse2, cnt2 = oracle.fwd(q, k, v, 19, 0, 0.25, lib=lib)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(cnt, cnt2)
+
+
+def _sink_cache(k, v, L, W, ns, S_slots, seed):
+    """Cache of ns sink slots then a W-slot ring for positions >= ns (p at ns + (p-ns) % W),
+    holding tokens 0..L-1 of k/v [B,L,Hkv,D]; built here without the oracle."""
+    B, _, Hkv, D = k.shape
+    kc = I.normal_bf16(seed, (B, Hkv, S_slots, D))
+    vc = I.normal_bf16(seed + 1, (B, Hkv, S_slots, D))
+    pos = np.full((B, S_slots), -1, dtype=np.int32)
+    for p in range(L):
+        if p < ns:
+            j = p
+        elif p > L - 1 - W:
+            j = ns + (p - ns) % W
+        else:
+            continue
+        pos[:, j] = p
+        kc[:, :, j] = k[:, p]
+        vc[:, :, j] = v[:, p]
+    return kc, vc, pos
+
+
+def check_decode_sinks(lib):
+    # Decode with the first ns positions pinned equals row t of the sink prefill.
+    for L, W, ns in [(30, 8, 2), (9, 8, 3), (3, 8, 2), (50, 4, 4)]:
+        B, Hq, Hkv, D = 2, 4, 2, 16
+        q, k, v = _rand_case(100 + L, B, L, Hq, Hkv, D)
+        o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, W - 1, 0, 0.25, list(range(ns)), lib=lib,
+                                             gmode=oracle.GLOBAL_SINK)
+        kc, vc, pos = _sink_cache(k, v, L, W, ns, ns + W, 700 + L)
+        o, lse, cnt = oracle.decode(q[:, L - 1], kc, vc, pos, np.array([L - 1] * B), 0.25, lib=lib, window=W,
+                                    n_sink=ns)
+        np.testing.assert_allclose(o, o_ref[:, :, L - 1], atol=1e-12, rtol=1e-10)
+        np.testing.assert_allclose(lse, lse_ref[:, :, L - 1], atol=1e-12, rtol=1e-10)
+        np.testing.assert_array_equal(cnt, min(L, W) + max(0, min(ns, L - W)))
+
+
+# ----------------------------------------------------------------------------- global projections
+def check_global_projection_identity(lib):
+    # With Q_g = Q, K_g = K, V_g = V the two-projection design is the one-projection
+    # attention (Longformer page 5.3: the global projections start as copies).
+    q, k, v = _rand_case(110, 2, 30, 4, 2, 16)
+    G = [0, 7, 29]
+    o, lse, cnt = oracle.fwd(q, k, v, 3, 3, 0.25, G, lib=lib)
+    o2, lse2, cnt2 = oracle.fwd(q, k, v, 3, 3, 0.25, G, lib=lib, qg=q, kg=k, vg=v)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    np.testing.assert_array_equal(cnt, cnt2)
+
+
+def check_global_projection_roles(lib):
+    q, k, v = _rand_case(111, 1, 30, 4, 2, 16)
+    qg, kg, vg = _rand_case(112, 1, 30, 4, 2, 16)
+    G = [0, 12]
+    o, lse, _ = oracle.fwd(q, k, v, 2, 2, 0.25, G, lib=lib, qg=qg, kg=kg, vg=vg)
+    ob, lseb, _ = oracle.dense_bruteforce(q, k, v, 2, 2, 0.25, G, qg=qg, kg=kg, vg=vg)
+    np.testing.assert_allclose(o, ob, atol=1e-12, rtol=1e-10)
+    np.testing.assert_allclose(lse, lseb, atol=1e-12, rtol=1e-10)
+    # Global rows read only Q_g, K_g, V_g: replacing Q, K, V leaves them unchanged.
+    q2, k2, v2 = _rand_case(113, 1, 30, 4, 2, 16)
+    o2, lse2, _ = oracle.fwd(q2, k2, v2, 2, 2, 0.25, G, lib=lib, qg=qg, kg=kg, vg=vg)
+    np.testing.assert_array_equal(o2[:, :, G], o[:, :, G])
+    np.testing.assert_array_equal(lse2[:, :, G], lse[:, :, G])
+    # Local rows read Q_g nowhere and K_g, V_g only at global positions.
+    loc = [t for t in range(30) if t not in G]
+    qg3, kg3, vg3 = _rand_case(114, 1, 30, 4, 2, 16)
+    kg3[:, G], vg3[:, G] = kg[:, G], vg[:, G]
+    o3, lse3, _ = oracle.fwd(q, k, v, 2, 2, 0.25, G, lib=lib, qg=qg3, kg=kg3, vg=vg3)
+    np.testing.assert_array_equal(o3[:, :, loc], o[:, :, loc])
+    # ... and they do read K_g, V_g at a global position, even inside their band.
+    kg4 = kg.copy()
+    kg4[:, 12] = k[:, 12]
+    o4, _, _ = oracle.fwd(q, k, v, 2, 2, 0.25, G, lib=lib, qg=qg, kg=kg4, vg=vg)
+    assert np.abs(o4[:, :, 11] - o[:, :, 11]).max() > 1e-6
+
+
+# ----------------------------------------------------------------------------- ring append, chunks
+def _ring_closed_form(L, W):
+    """Slot positions after tokens 0..L-1 went into slot p mod W: the largest
+    p <= L-1 with p = j (mod W), or -1 for a slot never written."""
+    j = np.arange(W)
+    last = L - 1 - ((L - 1 - j) % W)
+    return np.where(j < L, last, -1) if L < W else last
+
+
+def check_append_ring(lib):
+    B, Hkv, D, W = 2, 2, 8, 8
+    for L, pieces in [(5, [5]), (8, [3, 5]), (21, [1, 6, 7, 7]), (30, [30]), (17, [16, 1])]:
+        k = I.normal_bf16(120 + L, (B, L, Hkv, D))
+        v = I.normal_bf16(121 + L, (B, L, Hkv, D))
+        kc = I.normal_bf16(122, (B, Hkv, W, D))
+        vc = I.normal_bf16(123, (B, Hkv, W, D))
+        pos = np.full((B, W), -1, dtype=np.int32)
+        p0 = 0
+        for n in pieces:
+            kc, vc, pos = oracle.cache_append(kc, vc, pos, k[:, p0:p0 + n], v[:, p0:p0 + n], [p0] * B, lib=lib)
+            p0 += n
+        want = _ring_closed_form(L, W)
+        for b in range(B):
+            np.testing.assert_array_equal(pos[b], want)
+            for j in range(W):
+                if want[j] >= 0:
+                    np.testing.assert_array_equal(kc[b, :, j], k[b, want[j]])
+                    np.testing.assert_array_equal(vc[b, :, j], v[b, want[j]])
+
+
+def check_chunk_matches_prefill(lib):
+    # Chunked prefill (history in the ring, chunk as new tokens) equals rows
+    # p0 .. p0+C-1 of the causal-window prefill over the whole sequence.
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    for p0, C, W in [(0, 5, 4), (3, 4, 8), (10, 6, 4), (20, 20, 8), (7, 1, 8), (16, 9, 16)]:
+        L = p0 + C
+        q, k, v = _rand_case(130 + L, B, L, Hq, Hkv, D)
+        o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, W - 1, 0, 0.25, lib=lib)
+        kc = I.normal_bf16(131, (B, Hkv, W, D))
+        vc = I.normal_bf16(132, (B, Hkv, W, D))
+        pos = np.full((B, W), -1, dtype=np.int32)
+        if p0:
+            kc, vc, pos = oracle.cache_append(kc, vc, pos, k[:, :p0], v[:, :p0], [0] * B, lib=lib)
+        o, lse, cnt = oracle.chunk(q[:, p0:], k[:, p0:], v[:, p0:], kc, vc, pos, [p0] * B, W, 0.25, lib=lib)
+        np.testing.assert_allclose(o, o_ref[:, :, p0:], atol=1e-12, rtol=1e-10)
+        np.testing.assert_allclose(lse, lse_ref[:, :, p0:], atol=1e-12, rtol=1e-10)
+        np.testing.assert_array_equal(cnt, cnt_ref[:, :, p0:])
+    # Slots holding positions at or after p0 (left by tokens that were rolled back)
+    # are not history: a cache of W+3 slots keeps the whole window even after three
+    # such tokens were appended, and the chunk must ignore them.
+    p0, C, W = 12, 5, 8
+    L = p0 + C
+    q, k, v = _rand_case(135, B, L, Hq, Hkv, D)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, W - 1, 0, 0.25, lib=lib)
+    kc = I.normal_bf16(136, (B, Hkv, W + 3, D))
+    vc = I.normal_bf16(137, (B, Hkv, W + 3, D))
+    pos = np.full((B, W + 3), -1, dtype=np.int32)
+    kc, vc, pos = oracle.cache_append(kc, vc, pos, k[:, :p0], v[:, :p0], [0] * B, lib=lib)
+    junk_k, junk_v = I.normal_bf16(138, (B, 3, Hkv, D), 3.0), I.normal_bf16(139, (B, 3, Hkv, D), 3.0)
+    kc, vc, pos = oracle.cache_append(kc, vc, pos, junk_k, junk_v, [p0] * B, lib=lib)
+    o, lse, cnt = oracle.chunk(q[:, p0:], k[:, p0:], v[:, p0:], kc, vc, pos, [p0] * B, W, 0.25, lib=lib)
+    np.testing.assert_allclose(o, o_ref[:, :, p0:], atol=1e-12, rtol=1e-10)
+    np.testing.assert_array_equal(cnt, cnt_ref[:, :, p0:])
+    # With pinned sinks, against the sink prefill.
+    p0, C, W, ns = 20, 6, 8, 2
+    L = p0 + C
+    q, k, v = _rand_case(140, B, L, Hq, Hkv, D)
+    o_ref, lse_ref, _ = oracle.fwd(q, k, v, W - 1, 0, 0.25, list(range(ns)), lib=lib, gmode=oracle.GLOBAL_SINK)
+    kc, vc, pos = _sink_cache(k, v, p0, W, ns, ns + W, 141)
+    o, lse, _ = oracle.chunk(q[:, p0:], k[:, p0:], v[:, p0:], kc, vc, pos, [p0] * B, W, 0.25, n_sink=ns, lib=lib)
+    np.testing.assert_allclose(o, o_ref[:, :, p0:], atol=1e-12, rtol=1e-10)
+    np.testing.assert_allclose(lse, lse_ref[:, :, p0:], atol=1e-12, rtol=1e-10)
+
+
 ALL_CHECKS = [
     check_n16_r2_rows,
     check_n16_globals,
@@ -322,4 +568,15 @@ ALL_CHECKS = [
     check_decode_matches_prefill,
     check_decode_guards,
     check_workload_counts,
+    check_dilated_n16_rows,
+    check_dilated_closed_forms,
+    check_dilated_residue_identity,
+    check_dilated_bruteforce,
+    check_sink_counts,
+    check_sink_bruteforce,
+    check_decode_sinks,
+    check_global_projection_identity,
+    check_global_projection_roles,
+    check_append_ring,
+    check_chunk_matches_prefill,
 ]
