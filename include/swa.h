@@ -15,13 +15,27 @@
  *             Windows to Global Context", section 1.1) is window_left =
  *             window_right = r.  Global positions (same page, section 4.3) attend
  *             to every key and are attended by every query; a global key already
- *             inside a query's band is counted once.
+ *             inside a query's band is counted once.  Variants:
+ *               - global_mode SWA_GLOBAL_SINK: the listed positions are attention
+ *                 sinks (lizeman page, "Failure mode 1", after StreamingLLM): key
+ *                 columns that every query sees unless they lie right of its band
+ *                 (for a causal window: in its future); their rows are ordinary.
+ *               - separate global projections q_g, k_g, v_g (prathamp.com page,
+ *                 section 5.2): a global row scores q_g[t] against k_g of every key
+ *                 and averages v_g; a local row scores q[t] against k_g, v_g at the
+ *                 global positions and against k, v elsewhere.
+ *               - dilation d per query head (same page, section 3.1; lizeman page,
+ *                 "Dilation"): the band becomes {t + k*d : -window_left <= k <=
+ *                 window_right}, clipped to [0, T); the window sides count steps
+ *                 of d.
  * swa_decode  One query token per sequence against a ring-buffer KV cache of W
  *             slots.  Token p is stored in slot p mod W (lizeman page, KV cache
  *             paragraph) and every slot carries its true token position; the
  *             window is evaluated on positions, not slot offsets (Gemma 3 note,
  *             ai-engineer-exhaustive.pages.dev, "How it works"): slot j is attended
- *             by the query at position t iff 0 <= pos_j and t - W < pos_j <= t.
+ *             by the query at position t iff 0 <= pos_j <= t and either
+ *             t - window < pos_j or pos_j < n_sink (the first n_sink positions
+ *             pinned as attention sinks; window defaults to W).
  *
  * Conventions
  * -----------
@@ -60,6 +74,10 @@ extern "C" {
 /* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
 typedef struct CUstream_st *swa_stream_t;
 
+/* Modes of swa_fwd's global position list. */
+#define SWA_GLOBAL_FULL 0 /* global tokens: their rows see every key, every row sees them */
+#define SWA_GLOBAL_SINK 1 /* attention sinks: key columns only, never right of a row's band */
+
 typedef enum swa_status {
     SWA_OK = 0,
     SWA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, stride or window */
@@ -78,8 +96,15 @@ typedef enum swa_status {
  *   row_counts  optional int32 [B, H_q, T], contiguous (NULL: not written).
  *   global_idx  optional int32 [n_global] device array of global positions, strictly
  *               increasing, each in [0, T) (NULL with n_global = 0: none).
+ *   global_mode SWA_GLOBAL_FULL (0) or SWA_GLOBAL_SINK (1): how global_idx is used.
+ *   q_g, k_g, v_g  optional separate global projections, laid out like q, k, v with
+ *               their own strides (all three or none; SWA_GLOBAL_FULL only).
+ *   dilation    optional HOST int32 [H_q]: band dilation of each query head, >= 1
+ *               (NULL: 1 for every head).  A dilation above 1 requires n_global = 0.
  * Requirements: d_h in {64, 128, 256}; H_q % H_kv == 0 and H_q / H_kv <= 16;
  * every base pointer 16-byte aligned; strides multiples of 8 elements; T >= 1.
+ * Fields after row_counts were added in ABI version 2; zero them for the version 1
+ * behaviour.
  */
 typedef struct swa_fwd_params {
     const void *q;
@@ -98,9 +123,17 @@ typedef struct swa_fwd_params {
     int64_t o_strides[3];
     float *lse;
     int32_t *row_counts;
+    int32_t global_mode;
+    const void *q_g;
+    const void *k_g;
+    const void *v_g;
+    int64_t qg_strides[3];
+    int64_t kg_strides[3];
+    int64_t vg_strides[3];
+    const int32_t *dilation;
 } swa_fwd_params;
 
-/* Bytes of device workspace swa_fwd needs (0 when n_global == 0); 0 for invalid params. */
+/* Bytes of device workspace swa_fwd needs (0 without global rows); 0 for invalid params. */
 SWA_API size_t swa_fwd_workspace_size(const swa_fwd_params *p);
 
 /*
@@ -115,13 +148,17 @@ SWA_API swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t work
 /*
  * swa_decode parameters (all contiguous).
  *   q          bf16 [B, H_q, d_h]    the current token's queries
- *   k_cache    bf16 [B, H_kv, W, d_h] ring buffers (the current token already stored)
+ *   k_cache    bf16 [B, H_kv, W, d_h] the W cache slots (the current token already stored)
  *   v_cache    bf16 [B, H_kv, W, d_h]
  *   slot_pos   int32 [B, W]  true token position held by each slot (< 0: never written)
  *   q_pos      int32 [B]     position t_b of the current token
  *   o          bf16 [B, H_q, d_h]
  *   lse        fp32 [B, H_q]
  *   row_counts optional int32 [B, H_q]
+ *   window     the window in positions, >= 0 (0: W)            (ABI version 2)
+ *   n_sink     positions 0 .. n_sink-1 are attended whatever the window, >= 0
+ *              (0: none); a cache with sinks keeps them in slots of their own
+ *              (see swa_cache_append)                          (ABI version 2)
  * Requirements: d_h in {64, 128, 256}; H_q % H_kv == 0 and H_q / H_kv <= 16; W >= 1;
  * pointers 16-byte aligned.
  */
@@ -136,6 +173,8 @@ typedef struct swa_decode_params {
     void *o;
     float *lse;
     int32_t *row_counts;
+    int32_t window;
+    int32_t n_sink;
 } swa_decode_params;
 
 /* Bytes of device workspace swa_decode needs (split partials); 0 for invalid params. */
@@ -193,7 +232,7 @@ SWA_API const char *swa_status_string(swa_status s);
 /* ABI version of this header (incremented on any layout change). */
 SWA_API int32_t swa_abi_version(void);
 
-#define SWA_ABI_VERSION 1
+#define SWA_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ __all__ = [
     "SwaError", "build", "load_library", "library_path",
     "swa_fwd", "swa_decode", "swa_fwd_workspace_size", "swa_decode_workspace_size",
     "swa_check_device_error", "swa_status_string", "swa_abi_version",
-    "SwaFwdParams", "SwaDecodeParams",
+    "SwaFwdParams", "SwaDecodeParams", "GLOBAL_FULL", "GLOBAL_SINK",
 ]
 
 _c_i64x3 = ctypes.c_int64 * 3
@@ -35,6 +35,9 @@ class SwaFwdParams(ctypes.Structure):
         ("d_h", ctypes.c_int32), ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
         ("scale", ctypes.c_float), ("global_idx", ctypes.c_void_p), ("n_global", ctypes.c_int32),
         ("o", ctypes.c_void_p), ("o_strides", _c_i64x3), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p),
+        ("global_mode", ctypes.c_int32), ("q_g", ctypes.c_void_p), ("k_g", ctypes.c_void_p), ("v_g", ctypes.c_void_p),
+        ("qg_strides", _c_i64x3), ("kg_strides", _c_i64x3), ("vg_strides", _c_i64x3),
+        ("dilation", ctypes.POINTER(ctypes.c_int32)),
     ]
 
 
@@ -47,8 +50,12 @@ class SwaDecodeParams(ctypes.Structure):
         ("B", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
         ("W", ctypes.c_int32), ("scale", ctypes.c_float),
         ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p),
+        ("window", ctypes.c_int32), ("n_sink", ctypes.c_int32),
     ]
 
+
+GLOBAL_FULL = 0  # global tokens: full rows and columns
+GLOBAL_SINK = 1  # attention sinks: key columns only, never right of a row's band
 
 STATUS = {0: "SWA_OK", 1: "SWA_ERR_INVALID_ARG", 2: "SWA_ERR_UNSUPPORTED", 3: "SWA_ERR_CUDA",
           4: "SWA_ERR_TIMEOUT", 5: "SWA_ERR_WORKSPACE"}
@@ -134,8 +141,12 @@ def _check_bf16(name, t, ndim):
         raise ValueError(f"{name}: expected a CUDA bf16 tensor of rank {ndim} with a contiguous last dim")
 
 
-def fwd_params(q, k, v, window_left: int, window_right: int, scale: float, global_idx, o, lse, row_counts):
-    """Fill a SwaFwdParams from tensors (q/k/v/o [B,T,H,d] bf16; lse/row_counts [B,H_q,T])."""
+def fwd_params(q, k, v, window_left: int, window_right: int, scale: float, global_idx, o, lse, row_counts,
+               global_mode: int = GLOBAL_FULL, qkv_g=None, dilation=None):
+    """Fill a SwaFwdParams from tensors (q/k/v/o [B,T,H,d] bf16; lse/row_counts [B,H_q,T]).
+
+    qkv_g: optional (q_g, k_g, v_g) separate global projections; dilation: optional
+    per-query-head list of band dilations (host ints)."""
     B, T, Hq, D = q.shape
     p = SwaFwdParams()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
@@ -150,6 +161,17 @@ def fwd_params(q, k, v, window_left: int, window_right: int, scale: float, globa
     p.n_global = 0 if global_idx is None else int(global_idx.numel())
     p.lse = lse.data_ptr()
     p.row_counts = None if row_counts is None else row_counts.data_ptr()
+    p.global_mode = int(global_mode)
+    if qkv_g is not None:
+        qg, kg, vg = qkv_g
+        p.q_g, p.k_g, p.v_g = qg.data_ptr(), kg.data_ptr(), vg.data_ptr()
+        p.qg_strides = _c_i64x3(*qg.stride()[:3])
+        p.kg_strides = _c_i64x3(*kg.stride()[:3])
+        p.vg_strides = _c_i64x3(*vg.stride()[:3])
+    if dilation is not None:
+        arr = (ctypes.c_int32 * Hq)(*[int(x) for x in dilation])
+        p._dilation_keepalive = arr  # the C call reads it through the pointer
+        p.dilation = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
     return p
 
 
@@ -158,12 +180,16 @@ def swa_fwd_workspace_size(params: SwaFwdParams) -> int:
 
 
 def swa_fwd(q, k, v, window_left: int, window_right: int, scale: float | None = None, global_idx=None, *,
-            o=None, lse=None, row_counts=None, want_counts: bool = False, workspace=None, stream=None):
+            o=None, lse=None, row_counts=None, want_counts: bool = False, workspace=None, stream=None,
+            global_mode: int = GLOBAL_FULL, q_g=None, k_g=None, v_g=None, dilation=None):
     """Banded attention over q [B,T,H_q,d], k/v [B,T,H_kv,d] (bf16, CUDA).
 
     Keys s with t - window_left <= s <= t + window_right (negative: unbounded side),
-    plus global positions (int32 CUDA tensor, strictly increasing).  Returns
-    (o [B,T,H_q,d] bf16, lse [B,H_q,T] fp32, row_counts [B,H_q,T] int32 or None).
+    plus global positions (int32 CUDA tensor, strictly increasing) used as
+    global_mode says (GLOBAL_FULL rows and columns, GLOBAL_SINK pinned columns).
+    q_g, k_g, v_g: separate global projections (shapes of q, k, v).  dilation:
+    per-query-head band dilations (ints >= 1; window sides then count steps).
+    Returns (o [B,T,H_q,d] bf16, lse [B,H_q,T] fp32, row_counts [B,H_q,T] int32 or None).
     """
     import torch
 
@@ -183,7 +209,19 @@ def swa_fwd(q, k, v, window_left: int, window_right: int, scale: float | None = 
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None else lse
     if row_counts is None and want_counts:
         row_counts = torch.empty((B, Hq, T), dtype=torch.int32, device=q.device)
-    p = fwd_params(q, k, v, window_left, window_right, scale, global_idx, o, lse, row_counts)
+    qkv_g = None
+    if q_g is not None or k_g is not None or v_g is not None:
+        if q_g is None or k_g is None or v_g is None:
+            raise ValueError("q_g, k_g and v_g go together")
+        for name, t, ref in (("q_g", q_g, q), ("k_g", k_g, k), ("v_g", v_g, v)):
+            _check_bf16(name, t, 4)
+            if t.shape != ref.shape:
+                raise ValueError(f"{name}: expected shape {tuple(ref.shape)}")
+        qkv_g = (q_g, k_g, v_g)
+    if dilation is not None and len(dilation) != Hq:
+        raise ValueError(f"dilation: expected {Hq} entries")
+    p = fwd_params(q, k, v, window_left, window_right, scale, global_idx, o, lse, row_counts, global_mode, qkv_g,
+                   dilation)
     need = int(lib.swa_fwd_workspace_size(ctypes.byref(p)))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -195,7 +233,8 @@ def swa_fwd(q, k, v, window_left: int, window_right: int, scale: float | None = 
     return o, lse, row_counts
 
 
-def decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale: float, o, lse, row_counts):
+def decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale: float, o, lse, row_counts, window: int = 0,
+                  n_sink: int = 0):
     B, Hq, D = q.shape
     p = SwaDecodeParams()
     p.q, p.k_cache, p.v_cache = q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr()
@@ -204,6 +243,7 @@ def decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale: float, o, lse, ro
     p.scale = float(scale)
     p.o, p.lse = o.data_ptr(), lse.data_ptr()
     p.row_counts = None if row_counts is None else row_counts.data_ptr()
+    p.window, p.n_sink = int(window), int(n_sink)
     return p
 
 
@@ -212,10 +252,13 @@ def swa_decode_workspace_size(params: SwaDecodeParams) -> int:
 
 
 def swa_decode(q, k_cache, v_cache, slot_pos, q_pos, scale: float | None = None, *, o=None, lse=None,
-               row_counts=None, want_counts: bool = False, workspace=None, stream=None):
+               row_counts=None, want_counts: bool = False, workspace=None, stream=None, window: int = 0,
+               n_sink: int = 0):
     """Ring-buffer decode: q [B,H_q,d], caches [B,H_kv,W,d] (bf16), slot_pos [B,W], q_pos [B] (int32).
 
-    Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32, row_counts [B,H_q] int32 or None).
+    window: the window in positions (0: the number of slots W); n_sink: the first
+    positions that are always attended.  Returns (o [B,H_q,d] bf16, lse [B,H_q] fp32,
+    row_counts [B,H_q] int32 or None).
     """
     import torch
 
@@ -235,7 +278,7 @@ def swa_decode(q, k_cache, v_cache, slot_pos, q_pos, scale: float | None = None,
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
     if row_counts is None and want_counts:
         row_counts = torch.empty((B, Hq), dtype=torch.int32, device=q.device)
-    p = decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale, o, lse, row_counts)
+    p = decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale, o, lse, row_counts, window, n_sink)
     need = int(lib.swa_decode_workspace_size(ctypes.byref(p)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

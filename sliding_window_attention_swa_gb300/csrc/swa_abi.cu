@@ -26,6 +26,9 @@ bool failed(cudaError_t e) {
     return true;
 }
 
+// Separate global projections given (all three) or not (none); a partial set is invalid.
+bool has_sep(const swa_fwd_params *p) { return p->q_g || p->k_g || p->v_g; }
+
 swa_status fwd_check(const swa_fwd_params *p) {
     if (!p || !p->q || !p->k || !p->v || !p->o || !p->lse) return SWA_ERR_INVALID_ARG;
     if (p->B < 1 || p->T < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1) return SWA_ERR_INVALID_ARG;
@@ -33,6 +36,21 @@ swa_status fwd_check(const swa_fwd_params *p) {
     if (p->n_global < 0 || p->n_global > p->T) return SWA_ERR_INVALID_ARG;
     if (p->n_global > 0 && !p->global_idx) return SWA_ERR_INVALID_ARG;
     if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
+    if (p->global_mode != SWA_GLOBAL_FULL && p->global_mode != SWA_GLOBAL_SINK) return SWA_ERR_INVALID_ARG;
+    if (has_sep(p)) {
+        if (!p->q_g || !p->k_g || !p->v_g || p->global_mode != SWA_GLOBAL_FULL) return SWA_ERR_INVALID_ARG;
+        if (!strides_ok(p->qg_strides) || !strides_ok(p->kg_strides) || !strides_ok(p->vg_strides) ||
+            !aligned16(p->q_g) || !aligned16(p->k_g) || !aligned16(p->v_g))
+            return SWA_ERR_UNSUPPORTED;
+    }
+    if (p->dilation) {
+        bool dilated = false;
+        for (int h = 0; h < p->H_q; ++h) {
+            if (p->dilation[h] < 1) return SWA_ERR_INVALID_ARG;
+            dilated |= p->dilation[h] > 1;
+        }
+        if (dilated && p->n_global > 0) return SWA_ERR_UNSUPPORTED;
+    }
     if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
     if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
     if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
@@ -52,6 +70,7 @@ swa_status decode_check(const swa_decode_params *p) {
     if (p->B < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1 || p->W < 1) return SWA_ERR_INVALID_ARG;
     if (p->H_q % p->H_kv != 0) return SWA_ERR_INVALID_ARG;
     if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
+    if (p->window < 0 || p->n_sink < 0) return SWA_ERR_INVALID_ARG;
     if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
     if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
     if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
@@ -68,10 +87,141 @@ swa_status workspace_ok(void *ws, size_t have, size_t need) {
     return SWA_OK;
 }
 
+// Global rows (attending to every key) exist only for SWA_GLOBAL_FULL.
+bool has_global_rows(const swa_fwd_params *p) { return p->n_global > 0 && p->global_mode == SWA_GLOBAL_FULL; }
+
+// Band launches of swa_fwd.  A dilated head attends, within each residue class
+// t = r (mod d), to the ordinary band of that subsequence (keys t + k*d), so every
+// (dilation, residue) pair is one launch over strided views of q, k, v, o, lse and
+// counts: token stride d * stride, T' = ceil((T - r) / d), window sides unchanged.
+// Heads sharing a dilation are taken in runs of whole GQA groups; a head whose
+// group mixes dilations is launched alone (one query head over its kv head).
+cudaError_t launch_band_views(const swa_fwd_params *p, const swa::BandArgs &base, cudaStream_t s) {
+    auto dil = [&](int h) { return p->dilation ? p->dilation[h] : 1; };
+    const int G = p->H_q / p->H_kv;
+    bool uniform = true;
+    for (int h = 1; h < p->H_q; ++h) uniform &= dil(h) == dil(0);
+    if (uniform && dil(0) == 1) return swa::launch_band(base, s);
+    auto launch = [&](int h0, int nh, int kvh0, int nkv, int d) -> cudaError_t {
+        for (int r = 0; r < d && r < p->T; ++r) {
+            swa::BandArgs v = base;
+            const auto *q = static_cast<const uint16_t *>(p->q);
+            const auto *k = static_cast<const uint16_t *>(p->k);
+            const auto *vv = static_cast<const uint16_t *>(p->v);
+            auto *o = static_cast<uint16_t *>(p->o);
+            v.q = q + r * p->q_strides[1] + static_cast<int64_t>(h0) * p->q_strides[2];
+            v.k = k + r * p->k_strides[1] + static_cast<int64_t>(kvh0) * p->k_strides[2];
+            v.v = vv + r * p->v_strides[1] + static_cast<int64_t>(kvh0) * p->v_strides[2];
+            v.o = o + r * p->o_strides[1] + static_cast<int64_t>(h0) * p->o_strides[2];
+            v.q_st[1] = d * p->q_strides[1];
+            v.k_st[1] = d * p->k_strides[1];
+            v.v_st[1] = d * p->v_strides[1];
+            v.o_st[1] = d * p->o_strides[1];
+            v.T = (p->T - r + d - 1) / d;
+            v.H_q = nh;
+            v.H_kv = nkv;
+            const int64_t off = static_cast<int64_t>(h0) * base.lse_st[1] + r * base.lse_st[2];
+            v.lse = p->lse + off;
+            v.counts = p->row_counts ? p->row_counts + off : nullptr;
+            v.lse_st[2] = d * base.lse_st[2];
+            const cudaError_t e = swa::launch_band(v, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    };
+    int g = 0;
+    while (g < p->H_kv) {
+        bool whole = true;
+        for (int h = g * G + 1; h < (g + 1) * G; ++h) whole &= dil(h) == dil(g * G);
+        if (!whole) {
+            for (int h = g * G; h < (g + 1) * G; ++h) {
+                const cudaError_t e = launch(h, 1, g, 1, dil(h));
+                if (e != cudaSuccess) return e;
+            }
+            ++g;
+            continue;
+        }
+        int g1 = g + 1;  // extend the run over following whole groups of the same dilation
+        while (g1 < p->H_kv) {
+            bool same = true;
+            for (int h = g1 * G; h < (g1 + 1) * G; ++h) same &= dil(h) == dil(g * G);
+            if (!same) break;
+            ++g1;
+        }
+        const cudaError_t e = launch(g * G, (g1 - g) * G, g, g1 - g, dil(g * G));
+        if (e != cudaSuccess) return e;
+        g = g1;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 swa_status swa::validate_decode(const swa_decode_params *p) { return decode_check(p); }
 bool swa::record_cuda_failure(cudaError_t e) { return failed(e); }
+
+size_t swa::decode_workspace_bytes(const swa_decode_params *p) {
+    return split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, p->W);
+}
+
+cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s) {
+    const int64_t D = p->d_h, W = p->W;
+    SplitArgs sa{};
+    sa.q = p->q;
+    sa.q_sb = static_cast<int64_t>(p->H_q) * D;
+    sa.q_st = 0;
+    sa.q_sh = D;
+    sa.k = p->k_cache;
+    sa.v = p->v_cache;
+    sa.k_sb = sa.v_sb = static_cast<int64_t>(p->H_kv) * W * D;
+    sa.k_ss = sa.v_ss = D;
+    sa.k_sh = sa.v_sh = W * D;
+    sa.slot_pos = p->slot_pos;
+    sa.q_pos = p->q_pos;
+    sa.q_tok = nullptr;
+    sa.tok_limit = 1;
+    sa.B = p->B;
+    sa.NQ = 1;
+    sa.H_q = p->H_q;
+    sa.H_kv = p->H_kv;
+    sa.D = p->d_h;
+    sa.n_slots = p->W;
+    sa.W = p->window > 0 ? p->window : p->W;
+    sa.n_sink = p->n_sink;
+    sa.scale_log2 = p->scale * kLog2e;
+    sa.slots_per_split = kSlotsPerSplit;
+    sa.n_splits = split_count(p->W);
+    sa.q_per_cta = split_q_per_cta(p->H_q / p->H_kv);
+    split_carve(ws, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
+    cudaError_t e = launch_split(sa, s);
+    if (e != cudaSuccess) return e;
+
+    MergeArgs ma{};
+    ma.ws_ml = sa.ws_ml;
+    ma.ws_acc = sa.ws_acc;
+    ma.ws_cnt = sa.ws_cnt;
+    ma.B = p->B;
+    ma.NQ = 1;
+    ma.H_q = p->H_q;
+    ma.H_kv = p->H_kv;
+    ma.D = p->d_h;
+    ma.n_splits = sa.n_splits;
+    ma.q_tok = nullptr;
+    ma.tok_limit = 1;
+    ma.o = p->o;
+    ma.o_sb = static_cast<int64_t>(p->H_q) * D;
+    ma.o_st = 0;
+    ma.o_sh = D;
+    ma.lse = p->lse;
+    ma.lse_sb = p->H_q;
+    ma.lse_sh = 1;
+    ma.lse_st = 0;
+    ma.counts = p->row_counts;
+    ma.cnt_sb = p->H_q;
+    ma.cnt_sh = 1;
+    ma.cnt_st = 0;
+    return launch_merge(ma, s);
+}
 
 extern "C" {
 
@@ -92,7 +242,7 @@ const char *swa_status_string(swa_status s) {
 }
 
 size_t swa_fwd_workspace_size(const swa_fwd_params *p) {
-    if (fwd_check(p) != SWA_OK || p->n_global == 0) return 0;
+    if (fwd_check(p) != SWA_OK || !has_global_rows(p)) return 0;
     return swa::split_workspace_bytes(p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T);
 }
 
@@ -103,6 +253,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
     if (st != SWA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float scale_log2 = p->scale * kLog2e;
+    const bool sep = has_sep(p);
 
     swa::BandArgs ba{};
     ba.q = p->q;
@@ -114,6 +265,8 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         ba.k_st[i] = p->k_strides[i];
         ba.v_st[i] = p->v_strides[i];
         ba.o_st[i] = p->o_strides[i];
+        ba.kg_st[i] = sep ? p->kg_strides[i] : p->k_strides[i];
+        ba.vg_st[i] = sep ? p->vg_strides[i] : p->v_strides[i];
     }
     ba.B = p->B;
     ba.T = p->T;
@@ -125,26 +278,38 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
     ba.scale_log2 = scale_log2;
     ba.global_idx = p->n_global > 0 ? p->global_idx : nullptr;
     ba.n_global = p->n_global;
+    ba.gmode = p->global_mode;
+    ba.sep = sep && p->n_global > 0;
+    ba.kg = sep ? p->k_g : p->k;
+    ba.vg = sep ? p->v_g : p->v;
     ba.lse = p->lse;
     ba.counts = p->row_counts;
-    if (failed(swa::launch_band(ba, s))) return SWA_ERR_CUDA;
+    ba.lse_st[0] = static_cast<int64_t>(p->H_q) * p->T;
+    ba.lse_st[1] = p->T;
+    ba.lse_st[2] = 1;
+    if (failed(launch_band_views(p, ba, s))) return SWA_ERR_CUDA;
 
-    if (p->n_global > 0) {
+    if (has_global_rows(p)) {
         // Global rows attend to all T keys: split-K over T, merged by log-sum-exp,
-        // overwriting the rows the band kernel wrote for those positions.
+        // overwriting the rows the band kernel wrote for those positions.  With
+        // separate projections they read q_g, k_g and v_g only.
+        const void *gq = sep ? p->q_g : p->q, *gk = sep ? p->k_g : p->k, *gv = sep ? p->v_g : p->v;
+        const int64_t *qs = sep ? p->qg_strides : p->q_strides;
+        const int64_t *ks = sep ? p->kg_strides : p->k_strides;
+        const int64_t *vs = sep ? p->vg_strides : p->v_strides;
         swa::SplitArgs sa{};
-        sa.q = p->q;
-        sa.q_sb = p->q_strides[0];
-        sa.q_st = p->q_strides[1];
-        sa.q_sh = p->q_strides[2];
-        sa.k = p->k;
-        sa.v = p->v;
-        sa.k_sb = p->k_strides[0];
-        sa.k_ss = p->k_strides[1];
-        sa.k_sh = p->k_strides[2];
-        sa.v_sb = p->v_strides[0];
-        sa.v_ss = p->v_strides[1];
-        sa.v_sh = p->v_strides[2];
+        sa.q = gq;
+        sa.q_sb = qs[0];
+        sa.q_st = qs[1];
+        sa.q_sh = qs[2];
+        sa.k = gk;
+        sa.v = gv;
+        sa.k_sb = ks[0];
+        sa.k_ss = ks[1];
+        sa.k_sh = ks[2];
+        sa.v_sb = vs[0];
+        sa.v_ss = vs[1];
+        sa.v_sh = vs[2];
         sa.slot_pos = nullptr;
         sa.q_pos = nullptr;
         sa.q_tok = p->global_idx;
@@ -156,6 +321,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         sa.D = p->d_h;
         sa.n_slots = p->T;
         sa.W = p->T;
+        sa.n_sink = 0;
         sa.scale_log2 = scale_log2;
         sa.slots_per_split = swa::kSlotsPerSplit;
         sa.n_splits = swa::split_count(p->T);
@@ -194,7 +360,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
 
 size_t swa_decode_workspace_size(const swa_decode_params *p) {
     if (decode_check(p) != SWA_OK) return 0;
-    return swa::split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, p->W);
+    return swa::decode_workspace_bytes(p);
 }
 
 swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t workspace_bytes, swa_stream_t stream) {
@@ -202,62 +368,7 @@ swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t worksp
     if (st != SWA_OK) return st;
     st = workspace_ok(workspace, workspace_bytes, swa_decode_workspace_size(p));
     if (st != SWA_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t D = p->d_h, W = p->W;
-
-    swa::SplitArgs sa{};
-    sa.q = p->q;
-    sa.q_sb = static_cast<int64_t>(p->H_q) * D;
-    sa.q_st = 0;
-    sa.q_sh = D;
-    sa.k = p->k_cache;
-    sa.v = p->v_cache;
-    sa.k_sb = sa.v_sb = static_cast<int64_t>(p->H_kv) * W * D;
-    sa.k_ss = sa.v_ss = D;
-    sa.k_sh = sa.v_sh = W * D;
-    sa.slot_pos = p->slot_pos;
-    sa.q_pos = p->q_pos;
-    sa.q_tok = nullptr;
-    sa.tok_limit = 1;
-    sa.B = p->B;
-    sa.NQ = 1;
-    sa.H_q = p->H_q;
-    sa.H_kv = p->H_kv;
-    sa.D = p->d_h;
-    sa.n_slots = p->W;
-    sa.W = p->W;
-    sa.scale_log2 = p->scale * kLog2e;
-    sa.slots_per_split = swa::kSlotsPerSplit;
-    sa.n_splits = swa::split_count(p->W);
-    sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
-    swa::split_carve(workspace, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
-    if (failed(swa::launch_split(sa, s))) return SWA_ERR_CUDA;
-
-    swa::MergeArgs ma{};
-    ma.ws_ml = sa.ws_ml;
-    ma.ws_acc = sa.ws_acc;
-    ma.ws_cnt = sa.ws_cnt;
-    ma.B = p->B;
-    ma.NQ = 1;
-    ma.H_q = p->H_q;
-    ma.H_kv = p->H_kv;
-    ma.D = p->d_h;
-    ma.n_splits = sa.n_splits;
-    ma.q_tok = nullptr;
-    ma.tok_limit = 1;
-    ma.o = p->o;
-    ma.o_sb = static_cast<int64_t>(p->H_q) * D;
-    ma.o_st = 0;
-    ma.o_sh = D;
-    ma.lse = p->lse;
-    ma.lse_sb = p->H_q;
-    ma.lse_sh = 1;
-    ma.lse_st = 0;
-    ma.counts = p->row_counts;
-    ma.cnt_sb = p->H_q;
-    ma.cnt_sh = 1;
-    ma.cnt_st = 0;
-    if (failed(swa::launch_merge(ma, s))) return SWA_ERR_CUDA;
+    if (failed(swa::run_decode(p, workspace, reinterpret_cast<cudaStream_t>(stream)))) return SWA_ERR_CUDA;
     return SWA_OK;
 }
 

@@ -92,12 +92,40 @@ struct BandKernelArgs {
     float scale_log2;
     const int32_t *global_idx;
     int n_global;
-    const __nv_bfloat16 *k, *v;  // for the global-column gather
+    int sink;  // global columns are attention sinks: kept only left of a row's band
+    int sep;   // separate global projections: band tiles drop global columns, the
+               // global-column tiles keep all of them
+    const __nv_bfloat16 *k, *v;  // for the global-column gather (k_g, v_g when sep)
     int64_t k_st[3], v_st[3], o_st[3];
     __nv_bfloat16 *o;
     float *lse;
     int32_t *counts;
+    int64_t lse_st[3];
 };
+
+// Bit c of bits[] is set when key k0 + c (0 <= c < BN) is a global position; the
+// list is sorted, so a binary search finds its first entry >= k0.  Returns whether
+// any bit is set.
+template <int BN>
+__device__ __forceinline__ bool global_bits(const int32_t *g, int n, int k0, uint32_t (&bits)[BN / 32]) {
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) bits[i] = 0u;
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(g + mid) < k0) lo = mid + 1;
+        else hi = mid;
+    }
+    bool any = false;
+    for (int i = lo; i < n; ++i) {
+        const int c = __ldg(g + i) - k0;
+        if (c >= BN) break;
+#pragma unroll
+        for (int wd = 0; wd < BN / 32; ++wd) bits[wd] |= (c >> 5) == wd ? (1u << (c & 31)) : 0u;
+        any = true;
+    }
+    return any;
+}
 
 // Geometry of work unit u (units are numbered longest first).
 struct Unit {
@@ -459,6 +487,19 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         for (int c = 0; c < BN; ++c)
                             x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
                     }
+                    if (a.sep) {
+                        // with separate global projections a global key is scored (with
+                        // k_g) in the global-column tiles only: drop it here
+                        uint32_t gb[BN / 32];
+                        if (global_bits<BN>(a.global_idx, a.n_global, k0, gb)) {
+#pragma unroll
+                            for (int c = 0; c < BN; ++c) {
+                                const bool g = (gb[c >> 5] >> (c & 31)) & 1u;
+                                count -= (g && x[c] != -INFINITY) ? 1 : 0;
+                                x[c] = g ? -INFINITY : x[c];
+                            }
+                        }
+                    }
                 } else {
                     // global columns: each lane loads BN/32 of this tile's positions, shuffles
                     // broadcast them; keep the ones outside the row's band
@@ -473,7 +514,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
                         const int gs = __shfl_sync(0xffffffffu, gv[c >> 5], c & 31);
-                        const bool al = (gs >= 0) & (gs < a.T) & ((gs < lo_abs) | (gs > hi_abs));
+                        // kept: outside the row's band (sinks: left of it); with separate
+                        // projections every global key is scored here
+                        const bool outside = (gs < lo_abs) | ((gs > hi_abs) & !a.sink);
+                        const bool al = (gs >= 0) & (gs < a.T) & (outside | (a.sep != 0));
                         cnt4[c & 3] += al ? 1 : 0;
                         x[c] = al ? x[c] : -INFINITY;
                     }
@@ -585,7 +629,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_of(wg));
             if (row_ok) {
-                const int64_t li = (static_cast<int64_t>(w.b) * a.H_q + h) * a.T + t;
+                const int64_t li = static_cast<int64_t>(w.b) * a.lse_st[0] + static_cast<int64_t>(h) * a.lse_st[1] +
+                                   static_cast<int64_t>(t) * a.lse_st[2];
                 a.lse[li] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 if (a.counts) a.counts[li] = count;
             }
@@ -677,12 +722,15 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.scale_log2 = x.scale_log2;
     a.global_idx = x.global_idx;
     a.n_global = x.n_global;
-    a.k = static_cast<const __nv_bfloat16 *>(x.k);
-    a.v = static_cast<const __nv_bfloat16 *>(x.v);
+    a.sink = x.gmode == SWA_GLOBAL_SINK ? 1 : 0;
+    a.sep = x.sep ? 1 : 0;
+    a.k = static_cast<const __nv_bfloat16 *>(x.sep ? x.kg : x.k);
+    a.v = static_cast<const __nv_bfloat16 *>(x.sep ? x.vg : x.v);
     for (int i = 0; i < 3; ++i) {
-        a.k_st[i] = x.k_st[i];
-        a.v_st[i] = x.v_st[i];
+        a.k_st[i] = x.sep ? x.kg_st[i] : x.k_st[i];
+        a.v_st[i] = x.sep ? x.vg_st[i] : x.v_st[i];
         a.o_st[i] = x.o_st[i];
+        a.lse_st[i] = x.lse_st[i];
     }
     a.o = static_cast<__nv_bfloat16 *>(x.o);
     a.lse = x.lse;

@@ -11,8 +11,8 @@
 namespace swa {
 
 // One query row set attended against a list of key/value "slots".
-//   decode:      slots are the W ring-buffer slots, a slot is valid iff its stored
-//                position p satisfies 0 <= p and t - W < p <= t (t = q_pos[b]);
+//   decode:      slots are the cache slots, a slot is valid iff its stored position p
+//                satisfies 0 <= p <= t and (t - W < p or p < n_sink) (t = q_pos[b]);
 //   global rows: slots are the T key positions, all valid; the queries are the
 //                rows of the global positions (q_tok[qs]).
 // Rows packed into one CTA: q_per_cta query tokens x the H_q/H_kv heads of a group.
@@ -23,13 +23,14 @@ struct SplitArgs {
     const void *v;
     int64_t k_sb, k_ss, k_sh;     // key element address: b*k_sb + slot*k_ss + kvh*k_sh
     int64_t v_sb, v_ss, v_sh;     // value element address, likewise
-    const int32_t *slot_pos;      // [B, W] (decode) or nullptr (every slot < n_slots valid)
+    const int32_t *slot_pos;      // [B, n_slots] (decode) or nullptr (every slot < n_slots valid)
     const int32_t *q_pos;         // [B] (decode) or nullptr
     const int32_t *q_tok;         // [NQ] token of each query (global rows) or nullptr (token 0)
     int tok_limit;                // q_tok entries outside [0, tok_limit) are skipped
     int B, NQ, H_q, H_kv, D;
-    int n_slots;  // W (decode) or T (global rows)
+    int n_slots;  // cache slots (decode) or T (global rows)
     int W;        // window for the position test (decode)
+    int n_sink;   // positions below n_sink pass the position test whatever the window
     float scale_log2;
     int slots_per_split, n_splits, q_per_cta;
     float *ws_ml;     // [B, NQ, H_q, n_splits, 2]   (max in log2 units, sum)
@@ -92,14 +93,23 @@ struct BandArgs {
     float scale_log2;
     const int32_t *global_idx;
     int n_global;
+    int gmode;           // SWA_GLOBAL_FULL / SWA_GLOBAL_SINK
+    bool sep;            // separate global projections: global keys come from kg, vg only
+    const void *kg, *vg; // key/value rows of the global-column tiles (k, v unless sep)
+    int64_t kg_st[3], vg_st[3];
     void *o;
     float *lse;
     int32_t *counts;
+    int64_t lse_st[3];  // element strides (b, h, t) of lse and counts
 };
 cudaError_t launch_band(const BandArgs &a, cudaStream_t s);
 
 // Host-side helpers of the C ABI shared with the allocation-free decode entry point.
 swa_status validate_decode(const swa_decode_params *p);  // the checks swa_decode applies
+// Bytes of split partials a decode of `p` needs, and the split + merge launches of a
+// validated decode into workspace `ws` (at least that many bytes, 256-byte aligned).
+size_t decode_workspace_bytes(const swa_decode_params *p);
+cudaError_t run_decode(const swa_decode_params *p, void *ws, cudaStream_t s);
 bool record_cuda_failure(cudaError_t e);                  // true (and recorded) if e failed
 unsigned int band_read_clear_error();
 

@@ -139,7 +139,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
             const int b = item / (a.n_splits * Y);
             const int slot0 = split * a.slots_per_split;
             const int nslots = min(a.n_slots, slot0 + a.slots_per_split) - slot0;
-            const int32_t *row = a.slot_pos ? a.slot_pos + static_cast<int64_t>(b) * a.W + slot0 : nullptr;
+            const int32_t *row = a.slot_pos ? a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot0 : nullptr;
 #pragma unroll
             for (int i = 0; i < 2 * MAX_CHUNKS; ++i) {
                 const int si = i * 32 + lane;
@@ -161,7 +161,8 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 #pragma unroll
             for (int i = 0; i < 2 * MAX_CHUNKS; ++i) {
                 const int64_t p = pos_cur[i];
-                v[i] = pos_cur[i] != INT_MIN && (!a.slot_pos || (p >= 0 && p > t - a.W && p <= t));
+                v[i] = pos_cur[i] != INT_MIN &&
+                       (!a.slot_pos || (p >= 0 && p <= t && (p > t - a.W || p < a.n_sink)));
             }
             unsigned long long mask[MAX_CHUNKS];
             int count = 0;

@@ -3,6 +3,7 @@ and rejects invalid arguments before launching anything (no GPU needed)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -33,16 +34,30 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert swa.swa_abi_version() == 1
+    assert swa.swa_abi_version() == 2
     for s in range(6):
         assert swa.swa_status_string(s)
     assert "unknown" in swa.swa_status_string(99)
 
 
-def test_struct_sizes_match_header_layout():
-    # fields in declaration order, natural alignment (x86-64 and aarch64 LP64)
-    assert ctypes.sizeof(swa.SwaFwdParams) == 3 * 8 + 9 * 8 + 7 * 4 + 4 + 8 + 4 + 4 + 8 + 24 + 8 + 8
-    assert ctypes.sizeof(swa.SwaDecodeParams) == 5 * 8 + 6 * 4 + 3 * 8
+def test_struct_layout_matches_header(tmp_path):
+    # The C compiler's sizeof / offsetof of every field against the ctypes mirrors.
+    structs = {"swa_fwd_params": swa.SwaFwdParams, "swa_decode_params": swa.SwaDecodeParams}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "swa.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    for line in subprocess.check_output([str(exe)]).decode().splitlines():
+        cname, field, val = line.split()
+        py = structs[cname]
+        got = ctypes.sizeof(py) if field == "size" else getattr(py, field).offset
+        assert got == int(val), (cname, field, got, val)
 
 
 def _valid_fwd():
@@ -79,6 +94,14 @@ def _valid_decode():
     (lambda p: setattr(p, "scale", -1.0), 2),
     (lambda p: setattr(p, "q", 0x10008), 2),           # misaligned
     (lambda p: setattr(p, "k_strides", (ctypes.c_int64 * 3)(100, 10, 3)), 2),
+    (lambda p: setattr(p, "global_mode", 2), 1),
+    (lambda p: setattr(p, "q_g", 0x10000), 1),         # q_g without k_g, v_g
+    (lambda p: (setattr(p, "q_g", 0x10000), setattr(p, "k_g", 0x10000), setattr(p, "v_g", 0x10000),
+                setattr(p, "global_mode", 1)), 1),      # separate projections with sinks
+    (lambda p: (setattr(p, "q_g", 0x10000), setattr(p, "k_g", 0x10000), setattr(p, "v_g", 0x10000)), 2),
+    (lambda p: setattr(p, "dilation", (ctypes.c_int32 * 4)(1, 0, 1, 1)), 1),
+    (lambda p: (setattr(p, "dilation", (ctypes.c_int32 * 4)(1, 2, 1, 1)), setattr(p, "global_idx", 0x20000),
+                setattr(p, "n_global", 1)), 2),         # dilation with globals
 ])
 def test_fwd_rejects(lib, mutate, status):
     p = _valid_fwd()
@@ -97,6 +120,8 @@ def test_fwd_workspace_needed_for_globals(lib):
     assert lib.swa_fwd(ctypes.byref(p), None, 0, None) == 5
     assert lib.swa_fwd(ctypes.byref(p), ctypes.c_void_p(0x100000), need - 1, None) == 5
     assert lib.swa_fwd(ctypes.byref(p), ctypes.c_void_p(0x100010), need, None) == 5  # not 256-B aligned
+    p.global_mode = 1  # sinks: no global rows, no workspace
+    assert lib.swa_fwd_workspace_size(ctypes.byref(p)) == 0
 
 
 @pytest.mark.parametrize("mutate,status", [
@@ -105,6 +130,8 @@ def test_fwd_workspace_needed_for_globals(lib):
     (lambda p: setattr(p, "H_kv", 3), 1),
     (lambda p: setattr(p, "d_h", 80), 2),
     (lambda p: setattr(p, "v_cache", 0x10004), 2),
+    (lambda p: setattr(p, "window", -1), 1),
+    (lambda p: setattr(p, "n_sink", -2), 1),
 ])
 def test_decode_rejects(lib, mutate, status):
     p = _valid_decode()

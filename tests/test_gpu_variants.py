@@ -1,0 +1,200 @@
+"""Attention sinks, separate global projections, dilated bands and decode windows
+(through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from parity import assert_parity, i32_dev, to_dev, to_host_f64
+from sliding_window_attention_swa_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(seed, B, T, Hq, Hkv, d, scale=1.0):
+    q = I.normal_bf16(seed, (B, T, Hq, d), scale)
+    k = I.normal_bf16(seed + 1, (B, T, Hkv, d), scale)
+    v = I.normal_bf16(seed + 2, (B, T, Hkv, d))
+    return q, k, v
+
+
+def _run(q, k, v, wl, wr, scale, G=None, **kw):
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    for name in ("q_g", "k_g", "v_g"):
+        if kw.get(name) is not None:
+            kw[name] = to_dev(kw[name])
+    g = None if G is None else i32_dev(G)
+    o, lse, cnt = swa.swa_fwd(to_dev(q), to_dev(k), to_dev(v), wl, wr, scale, g, want_counts=True, **kw)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    return to_host_f64(o).transpose(0, 2, 1, 3), lse.cpu().numpy().astype(np.float64), cnt.cpu().numpy()
+
+
+# ----------------------------------------------------------------------------- sinks
+SINKS = [
+    # B, T, Hq, Hkv, d, wl, wr, sinks
+    (1, 300, 8, 2, 128, 63, 0, [0, 1, 2, 3]),
+    (2, 257, 4, 4, 64, 31, 0, [0]),
+    (1, 200, 4, 2, 256, 40, 0, [0, 1]),
+    (1, 500, 12, 12, 64, 32, 32, [0, 1, 2, 3]),
+    (1, 100, 4, 1, 128, 150, 0, [0, 1, 2, 3]),          # sinks inside every band
+    (1, 700, 4, 2, 128, 100, 0, list(range(150))),      # two global-column tiles
+    (1, 400, 2, 1, 64, 20, 3, [5, 77, 300]),            # sinks that are not the first tokens
+]
+
+
+@pytest.mark.parametrize("case", SINKS, ids=[f"T{c[1]}-d{c[4]}-wl{c[5]}-wr{c[6]}-n{len(c[7])}" for c in SINKS])
+def test_sinks(case):
+    B, T, Hq, Hkv, d, wl, wr, G = case
+    q, k, v = _inputs(3 * T + d, B, T, Hq, Hkv, d)
+    scale = d ** -0.5
+    o, lse, cnt = _run(q, k, v, wl, wr, scale, G, global_mode=oracle.GLOBAL_SINK)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, wl, wr, scale, G, gmode=oracle.GLOBAL_SINK)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, str(case))
+
+
+def test_sinks_full_size_mistral():
+    """Mistral-shape causal prefill with four pinned sinks: every row's count against
+    the closed form min(t+1, W) + max(0, min(4, t-W+1)), sampled rows' O and lse."""
+    cfg = I.MISTRAL
+    q, k, v = I.prefill_inputs(cfg)
+    G = [0, 1, 2, 3]
+    W = cfg.window_left + 1
+    o, lse, cnt = _run(q, k, v, cfg.window_left, 0, cfg.scale, G, global_mode=oracle.GLOBAL_SINK)
+    t = np.arange(cfg.T)
+    want = np.minimum(t + 1, W) + np.maximum(0, np.minimum(4, t - W + 1))
+    assert (cnt == want[None, None, :]).all()
+    rng = np.random.default_rng(5)
+    ts = sorted({0, 3, 4, W - 1, W, W + 1, W + 3, W + 4, cfg.T - 1} | set(int(x) for x in rng.integers(0, cfg.T, 40)))
+    rows = np.array([(0, int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, 0, cfg.scale, G, rows=rows,
+                                         gmode=oracle.GLOBAL_SINK)
+    b, h, tt = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_parity(o[b, h, tt], lse[b, h, tt], cnt[b, h, tt], o_ref, lse_ref, cnt_ref, "mistral+sinks")
+
+
+# ----------------------------------------------------------------------------- global projections
+SEP = [
+    # B, T, Hq, Hkv, d, wl, wr, G
+    (1, 500, 12, 12, 64, 32, 32, [0, 250, 499]),
+    (2, 300, 8, 2, 128, 40, 40, [3, 4, 5, 127, 128]),   # globals inside bands, at tile edges
+    (1, 260, 4, 2, 256, 20, 0, [0, 100]),
+    (1, 400, 4, 1, 64, 16, 16, list(range(0, 400, 3))),  # many globals, two global tiles
+]
+
+
+@pytest.mark.parametrize("case", SEP, ids=[f"T{c[1]}-d{c[4]}-wl{c[5]}-wr{c[6]}-g{len(c[7])}" for c in SEP])
+def test_separate_global_projections(case):
+    B, T, Hq, Hkv, d, wl, wr, G = case
+    q, k, v = _inputs(5 * T + d, B, T, Hq, Hkv, d)
+    qg, kg, vg = _inputs(5 * T + d + 100, B, T, Hq, Hkv, d)
+    scale = d ** -0.5
+    o, lse, cnt = _run(q, k, v, wl, wr, scale, G, q_g=qg, k_g=kg, v_g=vg)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, wl, wr, scale, G, qg=qg, kg=kg, vg=vg)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, str(case))
+
+
+def test_separate_projections_full_size_longformer():
+    cfg = I.LONGFORMER
+    q, k, v = I.prefill_inputs(cfg)
+    qg = I.normal_bf16(cfg.seed * 16 + 8, q.shape)
+    kg = I.normal_bf16(cfg.seed * 16 + 9, k.shape)
+    vg = I.normal_bf16(cfg.seed * 16 + 10, v.shape)
+    G = list(cfg.globals_)
+    o, lse, cnt = _run(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, q_g=qg, k_g=kg, v_g=vg)
+    rng = np.random.default_rng(9)
+    ts = sorted({0, 1, 255, 256, 257, 2047, 2048, 2049, 1792, 2304, cfg.T - 1} |
+                set(int(x) for x in rng.integers(0, cfg.T, 60)))
+    rows = np.array([(int(rng.integers(0, cfg.B)), int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, rows=rows,
+                                         qg=qg, kg=kg, vg=vg)
+    b, h, t = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_parity(o[b, h, t], lse[b, h, t], cnt[b, h, t], o_ref, lse_ref, cnt_ref, "longformer+Qg/Kg/Vg")
+
+
+# ----------------------------------------------------------------------------- dilation
+DIL = [
+    # B, T, Hq, Hkv, d, wl, wr, dilation per query head
+    (1, 400, 8, 8, 64, 16, 16, [1, 1, 1, 1, 1, 1, 2, 2]),   # Longformer page 3.6 mix
+    (2, 300, 8, 2, 128, 30, 0, [1, 1, 1, 1, 3, 3, 3, 3]),    # whole GQA groups share d
+    (1, 333, 4, 2, 128, 20, 20, [1, 2, 4, 4]),               # a group that mixes d
+    (1, 257, 2, 1, 256, 12, 3, [2, 2]),
+    (1, 100, 4, 2, 64, 7, 0, [8, 8, 8, 8]),
+]
+
+
+@pytest.mark.parametrize("case", DIL, ids=[f"T{c[1]}-d{c[4]}-wl{c[5]}-wr{c[6]}-dil{''.join(map(str, c[7]))}" for c in DIL])
+def test_dilation(case):
+    B, T, Hq, Hkv, d, wl, wr, dil = case
+    q, k, v = _inputs(11 * T + d, B, T, Hq, Hkv, d)
+    scale = d ** -0.5
+    o, lse, cnt = _run(q, k, v, wl, wr, scale, dilation=dil)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, wl, wr, scale, dilation=dil)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, str(case))
+
+
+def test_dilation_full_size_longformer():
+    """Longformer-shape encoder, heads 8-11 dilated by 2 (no globals): every row's
+    count against the residue-class closed form, sampled rows' O and lse."""
+    cfg = I.LONGFORMER
+    q, k, v = I.prefill_inputs(cfg)
+    dil = [1] * 8 + [2] * 4
+    r = cfg.window_left
+    o, lse, cnt = _run(q, k, v, r, r, cfg.scale, dilation=dil)
+    t = np.arange(cfg.T)
+    for h in range(cfg.Hq):
+        d = dil[h]
+        want = np.minimum(r, t // d) + np.minimum(r, (cfg.T - 1 - t) // d) + 1
+        assert (cnt[:, h] == want[None, :]).all(), h
+    rng = np.random.default_rng(13)
+    ts = sorted({0, 1, 255, 256, 511, 512, 513, cfg.T - 2, cfg.T - 1} | set(int(x) for x in rng.integers(0, cfg.T, 60)))
+    rows = np.array([(int(rng.integers(0, cfg.B)), int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, r, r, cfg.scale, rows=rows, dilation=dil)
+    b, h, tt = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert_parity(o[b, h, tt], lse[b, h, tt], cnt[b, h, tt], o_ref, lse_ref, cnt_ref, "longformer dilated")
+
+
+# ----------------------------------------------------------------------------- decode window / sinks
+def _sink_cache(k, v, L, W, ns):
+    """ns sink slots, then a W-slot ring of the positions >= ns (p at ns + (p-ns) % W)."""
+    B, _, Hkv, D = k.shape
+    S = ns + W
+    kc = I.normal_bf16(4242, (B, Hkv, S, D))
+    vc = I.normal_bf16(4243, (B, Hkv, S, D))
+    pos = np.full((B, S), -1, dtype=np.int32)
+    for b in range(B):
+        for p in range(L[b]):
+            if p < ns:
+                j = p
+            elif p > L[b] - 1 - W:
+                j = ns + (p - ns) % W
+            else:
+                continue
+            pos[b, j] = p
+            kc[b, :, j] = k[b, p]
+            vc[b, :, j] = v[b, p]
+    return kc, vc, pos
+
+
+@pytest.mark.parametrize("W,ns,d", [(64, 4, 128), (600, 2, 64), (100, 1, 256), (512, 0, 128)])
+def test_decode_sinks_and_window(W, ns, d):
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    B, Hq, Hkv = 6, 8, 2
+    L = np.array([1, 3, W, W + ns + 5, 3 * W + 7, 2000])[:B]
+    Tm = int(L.max())
+    k = I.normal_bf16(31 + d, (B, Tm, Hkv, d))
+    v = I.normal_bf16(32 + d, (B, Tm, Hkv, d))
+    q = I.normal_bf16(33 + d, (B, Hq, d))
+    kc, vc, pos = _sink_cache(k, v, L, W, ns)
+    qpos = (L - 1).astype(np.int32)
+    o, lse, cnt = swa.swa_decode(to_dev(q), to_dev(kc), to_dev(vc), i32_dev(pos), i32_dev(qpos), d ** -0.5,
+                                 want_counts=True, window=W, n_sink=ns)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o_ref, lse_ref, cnt_ref = oracle.decode(q, kc, vc, pos, qpos, d ** -0.5, window=W, n_sink=ns)
+    assert_parity(to_host_f64(o), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref, cnt_ref, f"W{W} ns{ns}")
+    want = np.minimum(L, W) + np.maximum(0, np.minimum(ns, L - W))
+    assert (cnt.cpu().numpy() == want[:, None]).all()
