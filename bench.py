@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 from sliding_window_attention_swa_gb300 import inputs as I  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
-KERNELS = {"band": "band_fwd_kernel", "split": "split_attn_kernel", "merge": "merge_kernel"}
+KERNELS = {"band": "band_fwd_kernel", "split": "stream_attn_kernel", "merge": "merge_kernel"}
 
 
 # ----------------------------------------------------------------------------- work counts
@@ -52,6 +52,46 @@ def prefill_pairs(cfg) -> int:
 
 def prefill_flops(cfg) -> float:
     return 4.0 * cfg.d * prefill_pairs(cfg)
+
+
+def variant_pairs(cfg, variant) -> int:
+    """Attended pairs of a prefill variant, closed form per row: sinks add the sink
+    positions left of each row's band; a dilated head of dilation d keeps, of the
+    band, the keys of its residue class, min(wl, t//d) + min(wr, (T-1-t)//d) + 1."""
+    T, wl, wr = cfg.T, cfg.window_left, cfg.window_right
+    t = np.arange(T, dtype=np.int64)
+    if variant.get("dilation") is not None:
+        total = 0
+        for d in variant["dilation"]:
+            left = t // d if wl < 0 else np.minimum(wl, t // d)
+            right = (T - 1 - t) // d if wr < 0 else np.minimum(wr, (T - 1 - t) // d)
+            total += int((left + right + 1).sum())
+        return total * cfg.B
+    if variant.get("sinks"):
+        lo = np.zeros(T, dtype=np.int64) if wl < 0 else np.maximum(0, t - wl)
+        hi = np.full(T, T - 1, dtype=np.int64) if wr < 0 else np.minimum(T - 1, t + wr)
+        S = np.asarray(variant["sinks"])
+        cnt = hi - lo + 1 + (S[None, :] < lo[:, None]).sum(axis=1)
+        return int(cnt.sum()) * cfg.B * cfg.Hq
+    return prefill_pairs(cfg)
+
+
+def band_launches(cfg, dilation) -> int:
+    """Band-kernel launches of one dilated swa_fwd call: d per run of whole GQA groups
+    sharing dilation d, d per head of a group that mixes dilations."""
+    if dilation is None or all(x == 1 for x in dilation):
+        return 1
+    G = cfg.Hq // cfg.Hkv
+    groups = [tuple(dilation[g * G:(g + 1) * G]) for g in range(cfg.Hkv)]
+    n, prev = 0, None
+    for grp in groups:
+        if len(set(grp)) > 1:
+            n += sum(grp)
+            prev = None
+        elif grp[0] != prev:
+            n += grp[0]
+            prev = grp[0]
+    return n
 
 
 def prefill_bytes(cfg) -> int:
@@ -166,54 +206,79 @@ def timed_steps(fn, steps: int, warmup: int, flush, stream, sampler=None):
     return np.array([a.elapsed_time(b) for a, b in ev])  # ms
 
 
-def measure_prefill(cfg, steps, warmup, device, flush, sampler=None):
+def measure_prefill(cfg, steps, warmup, device, flush, sampler=None, variant=None):
+    """variant: None, or {"sinks": [...]} (pinned sink columns), {"sep": True} (separate
+    global projections q_g, k_g, v_g for cfg's globals), {"dilation": [...]}."""
     import torch
     import sliding_window_attention_swa_gb300 as swa
 
+    variant = variant or {}
     q, k, v = I.prefill_inputs(cfg)
     qd, kd, vd = to_dev(q, device), to_dev(k, device), to_dev(v, device)
+    extra = {}
+    if variant.get("sep"):
+        for i, (name, a) in enumerate((("q_g", q), ("k_g", k), ("v_g", v))):
+            extra[name] = to_dev(I.normal_bf16(cfg.seed * 16 + 8 + i, a.shape), device)
     del q, k, v
-    g = torch.tensor(cfg.globals_, dtype=torch.int32, device=device) if cfg.globals_ else None
+    gl = variant.get("sinks") or list(cfg.globals_)
+    g = torch.tensor(gl, dtype=torch.int32, device=device) if gl else None
+    gmode = swa.GLOBAL_SINK if variant.get("sinks") else swa.GLOBAL_FULL
+    dil = variant.get("dilation")
     o = torch.empty_like(qd)
     lse = torch.empty((cfg.B, cfg.Hq, cfg.T), dtype=torch.float32, device=device)
-    p = swa.fwd_params(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o, lse, None)
+    qkv_g = (extra["q_g"], extra["k_g"], extra["v_g"]) if extra else None
+    p = swa.fwd_params(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o, lse, None, gmode, qkv_g, dil)
     need = swa.swa_fwd_workspace_size(p)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def run():
         swa.swa_fwd(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o=o, lse=lse, workspace=ws,
-                    stream=stream)
+                    stream=stream, global_mode=gmode, dilation=dil, **extra)
 
     ms = timed_steps(run, steps, warmup, flush, stream, sampler)
     swa.swa_check_device_error()
-    launches = 1 + (2 if cfg.globals_ else 0)
-    return {"ms": ms, "flops": prefill_flops(cfg), "bytes": prefill_bytes(cfg), "launches_per_step": launches,
-            "tensors": (qd, kd, vd, g, o, lse, ws)}
+    launches = band_launches(cfg, dil) + (2 if (gl and gmode == swa.GLOBAL_FULL) else 0)
+    nbytes = prefill_bytes(cfg) + (2 * sum(t.numel() for t in extra.values()) if extra else 0)
+    return {"ms": ms, "flops": 4.0 * cfg.d * variant_pairs(cfg, variant), "bytes": nbytes,
+            "launches_per_step": launches, "tensors": (qd, kd, vd, g, o, lse, ws)}
 
 
-def measure_decode(cfg, steps, warmup, device, flush):
+def measure_decode(cfg, steps, warmup, device, flush, n_sink: int = 0):
+    """n_sink > 0: a cache of n_sink pinned slots plus a W-slot ring (same lengths)."""
     import torch
     import sliding_window_attention_swa_gb300 as swa
 
     q, kc, vc, pos, qpos = I.decode_inputs(cfg)
     L = qpos.astype(np.int64) + 1
+    if n_sink:
+        pos = I.sink_ring_slot_positions(L, cfg.W, n_sink)
+        pad = I.normal_bf16(cfg.seed * 16 + 7, (cfg.B, cfg.Hkv, n_sink, cfg.d))
+        kc = np.concatenate([pad, kc], axis=2)
+        vc = np.concatenate([pad, vc], axis=2)
     qd, kd, vd = to_dev(q, device), to_dev(kc, device), to_dev(vc, device)
     del kc, vc
     posd = torch.from_numpy(pos).to(device)
     qposd = torch.from_numpy(qpos).to(device)
     o = torch.empty_like(qd)
     lse = torch.empty((cfg.B, cfg.Hq), dtype=torch.float32, device=device)
-    p = swa.decode_params(qd, kd, vd, posd, qposd, cfg.scale, o, lse, None)
+    p = swa.decode_params(qd, kd, vd, posd, qposd, cfg.scale, o, lse, None, cfg.W, n_sink)
     ws = torch.empty(swa.swa_decode_workspace_size(p), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def run():
-        swa.swa_decode(qd, kd, vd, posd, qposd, cfg.scale, o=o, lse=lse, workspace=ws, stream=stream)
+        swa.swa_decode(qd, kd, vd, posd, qposd, cfg.scale, o=o, lse=lse, workspace=ws, stream=stream,
+                       window=cfg.W, n_sink=n_sink)
 
     ms = timed_steps(run, steps, warmup, flush, stream)
     swa.swa_check_device_error()
-    return {"ms": ms, "flops": decode_flops(cfg, L), "bytes": decode_bytes(cfg, L), "launches_per_step": 2}
+    nbytes, flops = decode_bytes(cfg, L), decode_flops(cfg, L)
+    if n_sink:
+        # the sinks outside the window: their K/V and positions
+        extra = int(np.maximum(0, np.minimum(n_sink, L - cfg.W)).sum())
+        nbytes += extra * cfg.Hkv * cfg.d * 2 * 2 + cfg.B * n_sink * 4
+        flops += 4.0 * cfg.d * extra * cfg.Hq
+    return {"ms": ms, "flops": flops, "bytes": nbytes, "launches_per_step": 2}
 
 
 def measure_e2e_prefill(cfg, steps, warmup, device, dev_tensors):
@@ -402,7 +467,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, help="comma list of workloads: mistral,decode,gemma,longformer")
+    ap.add_argument("--only", default=None,
+                    help="comma list of workloads: mistral,decode,gemma,longformer,variants")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -417,7 +483,7 @@ def main():
     torch.cuda.set_device(device)
     swa.load_library()
     hbm_peak, bf16_peak, peak_kind = load_peaks()
-    only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer"}
+    only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer", "variants"}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def barrier():
@@ -469,6 +535,34 @@ def main():
             "ms_per_step": rms, "frac_of_bf16_peak": r["flops"] / (rms * 1e-3) / 1e12 / bf16_peak,
             "hbm_gbs": r["bytes"] / (rms * 1e-3) / 1e9, "frac_of_hbm_peak": r["bytes"] / (rms * 1e-3) / 1e9 / hbm_peak}
         gpu_launches += r["launches_per_step"] * max(20, args.steps // 4)
+
+    if "variants" in only:
+        # the pages' variants on the same workloads: four attention sinks on the Mistral
+        # shape, separate global projections and a dilation mix on the Longformer shape,
+        # and decode with four sink slots beside the ring
+        import dataclasses
+
+        lf_local = dataclasses.replace(I.LONGFORMER, globals_=(), name=I.LONGFORMER.name + "-no-globals")
+        vsteps = max(20, args.steps // 8)
+        for key, cfg, variant in (
+                ("mistral_sinks4", I.MISTRAL, {"sinks": [0, 1, 2, 3]}),
+                ("longformer_separate_global_projections", I.LONGFORMER, {"sep": True}),
+                ("longformer_dilation_heads8to11_d2", lf_local, {"dilation": [1] * 8 + [2] * 4})):
+            r = measure_prefill(cfg, vsteps, args.warmup, device, flush, variant=variant)
+            del r["tensors"]
+            rms = max_over_ranks(float(r["ms"].mean()))
+            secondary[key] = {
+                "workload": cfg.name, "variant": {k: (v if k != "sinks" else len(v)) for k, v in variant.items()},
+                "value": world * r["flops"] / (rms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": rms,
+                "frac_of_bf16_peak": r["flops"] / (rms * 1e-3) / 1e12 / bf16_peak,
+                "hbm_gbs": r["bytes"] / (rms * 1e-3) / 1e9}
+            gpu_launches += r["launches_per_step"] * vsteps
+        d = measure_decode(I.DECODE, vsteps, args.warmup, device, flush, n_sink=4)
+        dms = max_over_ranks(float(d["ms"].mean()))
+        secondary["decode_sinks4"] = {
+            "workload": I.DECODE.name, "variant": {"n_sink": 4}, "value": world * d["bytes"] / (dms * 1e-3) / 1e9,
+            "unit": "GB/s", "ms_per_step": dms, "frac_of_hbm_peak": d["bytes"] / (dms * 1e-3) / 1e9 / hbm_peak}
+        gpu_launches += d["launches_per_step"] * vsteps
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

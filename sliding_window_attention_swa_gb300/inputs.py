@@ -241,6 +241,27 @@ def ring_slot_positions(L: np.ndarray, W: int) -> np.ndarray:
     return pos.astype(np.int32)
 
 
+def sink_ring_slot_positions(L: np.ndarray, W: int, n_sink: int) -> np.ndarray:
+    """Slot positions of a cache with n_sink pinned slots and a W-slot ring, int32 [B, n_sink + W].
+
+    Slots 0 .. n_sink-1 hold positions 0 .. n_sink-1 (those below L); position
+    p >= n_sink lives in slot n_sink + (p - n_sink) mod W, and the ring holds the
+    last W positions of the sequence (t = L - 1) that are not sinks.  Slots never
+    written hold -1.
+    """
+    B = L.shape[0]
+    pos = np.full((B, n_sink + W), -1, dtype=np.int64)
+    j = np.arange(n_sink)[None, :]
+    pos[:, :n_sink] = np.where(j < L[:, None], j, -1)
+    r = np.arange(W)[None, :]
+    t = (L - 1).astype(np.int64)[:, None]
+    # largest p <= t with p >= n_sink and (p - n_sink) = r (mod W)
+    p = t - ((t - n_sink - r) % W)
+    ok = (p >= n_sink) & (p > t - W)
+    pos[:, n_sink:] = np.where(ok, p, -1)
+    return pos.astype(np.int32)
+
+
 def decode_inputs(cfg: DecodeConfig):
     """(q [B,Hq,d], k_cache [B,Hkv,W,d], v_cache [B,Hkv,W,d], slot_pos [B,W], q_pos [B])."""
     L = decode_lengths(cfg)
