@@ -64,6 +64,8 @@ def _bind(lib):
     lib.swa_oracle_decode_ex.restype = ctypes.c_int
     lib.swa_oracle_cache_append.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _I64, _P]
     lib.swa_oracle_cache_append.restype = ctypes.c_int
+    lib.swa_oracle_cache_append_ex.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _I64, _P]
+    lib.swa_oracle_cache_append_ex.restype = ctypes.c_int
     lib.swa_oracle_chunk.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
                                      ctypes.c_double, _P, _P, _P]
     lib.swa_oracle_chunk.restype = ctypes.c_int
@@ -188,9 +190,10 @@ def decode(q, k_cache, v_cache, slot_pos, q_pos, scale: float, lib=None, window=
     return o, lse, cnt
 
 
-def cache_append(k_cache, v_cache, slot_pos, k_new, v_new, p0, lib=None):
+def cache_append(k_cache, v_cache, slot_pos, k_new, v_new, p0, lib=None, n_sink: int = 0):
     """Ring append on copies: returns (k_cache, v_cache, slot_pos) after writing the n
-    tokens of k_new/v_new [B,n,Hkv,D] at positions p0[b] + i into slots p mod S."""
+    tokens of k_new/v_new [B,n,Hkv,D] at positions p0[b] + i into slots p mod S (with
+    n_sink pinned sinks: slot p below n_sink, n_sink + (p - n_sink) mod (S - n_sink) else)."""
     lib = lib or load()
     kc = np.array(k_cache, dtype=np.uint16, order="C", copy=True)
     vc = np.array(v_cache, dtype=np.uint16, order="C", copy=True)
@@ -200,7 +203,12 @@ def cache_append(k_cache, v_cache, slot_pos, k_new, v_new, p0, lib=None):
     B, Hkv, S, D = kc.shape
     n = kn.shape[1]
     assert kn.shape == (B, n, Hkv, D) and vn.shape == kn.shape and p.shape == (B,)
-    if lib.swa_oracle_cache_append(_ptr(kc), _ptr(vc), _ptr(sp), B, Hkv, S, D, _ptr(kn), _ptr(vn), n, _ptr(p)) != 0:
+    if n_sink == 0:
+        rc = lib.swa_oracle_cache_append(_ptr(kc), _ptr(vc), _ptr(sp), B, Hkv, S, D, _ptr(kn), _ptr(vn), n, _ptr(p))
+    else:
+        rc = lib.swa_oracle_cache_append_ex(_ptr(kc), _ptr(vc), _ptr(sp), B, Hkv, S, D, n_sink, _ptr(kn), _ptr(vn),
+                                            n, _ptr(p))
+    if rc != 0:
         raise ValueError("swa_oracle_cache_append rejected its arguments")
     return kc, vc, sp
 

@@ -49,7 +49,9 @@
  * first n_sink positions pinned as sinks.  The rest is steps 2-4.
  *
  * Ring append (lizeman page, KV cache paragraph, quoting Mistral 7B section 2):
- * token p is stored in slot p mod S, overwriting what was there.  Chunked
+ * token p is stored in slot p mod S, overwriting what was there.  A cache that
+ * pins n_sink sinks keeps position p < n_sink in slot p and rings the rest through
+ * the other S - n_sink slots: slot n_sink + (p - n_sink) mod (S - n_sink).  Chunked
  * prefill: C new tokens at positions p0 .. p0+C-1 attend to the cached history
  * (slots holding positions below p0) and to the chunk itself, under the decode
  * rule above.
@@ -265,17 +267,19 @@ int swa_oracle_decode(const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
 /*
  * Ring append.  Token i (0 <= i < n) of sequence b has position p = p0[b] + i; in
  * order of i its key and value rows (k_new, v_new: [B,n,Hkv,D]) are written to slot
- * p mod S of every kv head of the caches ([B,Hkv,S,D]) and slot_pos[b][p mod S] = p.
- * Returns -1 on a bad argument (a negative position).
+ * j(p) of every kv head of the caches ([B,Hkv,S,D]) and slot_pos[b][j(p)] = p, with
+ * j(p) = p for a sink (p < n_sink) and n_sink + (p - n_sink) mod (S - n_sink) else.
+ * Returns -1 on a bad argument (a negative position, no ring slot).
  */
-int swa_oracle_cache_append(uint16_t *kc, uint16_t *vc, int32_t *slot_pos, int64_t B, int64_t Hkv, int64_t S,
-                            int64_t D, const uint16_t *k_new, const uint16_t *v_new, int64_t n, const int32_t *p0) {
-    if (B < 0 || Hkv <= 0 || S <= 0 || D <= 0 || n < 0) return -1;
+int swa_oracle_cache_append_ex(uint16_t *kc, uint16_t *vc, int32_t *slot_pos, int64_t B, int64_t Hkv, int64_t S,
+                               int64_t D, int64_t n_sink, const uint16_t *k_new, const uint16_t *v_new, int64_t n,
+                               const int32_t *p0) {
+    if (B < 0 || Hkv <= 0 || S <= 0 || D <= 0 || n < 0 || n_sink < 0 || n_sink >= S) return -1;
     for (int64_t b = 0; b < B; ++b) {
         if (p0[b] < 0) return -1;
         for (int64_t i = 0; i < n; ++i) {
             const int64_t p = (int64_t)p0[b] + i;
-            const int64_t j = p % S;
+            const int64_t j = p < n_sink ? p : n_sink + (p - n_sink) % (S - n_sink);
             slot_pos[b * S + j] = (int32_t)p;
             for (int64_t h = 0; h < Hkv; ++h) {
                 memcpy(kc + ((b * Hkv + h) * S + j) * D, k_new + ((b * n + i) * Hkv + h) * D, sizeof(uint16_t) * D);
@@ -284,6 +288,11 @@ int swa_oracle_cache_append(uint16_t *kc, uint16_t *vc, int32_t *slot_pos, int64
         }
     }
     return 0;
+}
+
+int swa_oracle_cache_append(uint16_t *kc, uint16_t *vc, int32_t *slot_pos, int64_t B, int64_t Hkv, int64_t S,
+                            int64_t D, const uint16_t *k_new, const uint16_t *v_new, int64_t n, const int32_t *p0) {
+    return swa_oracle_cache_append_ex(kc, vc, slot_pos, B, Hkv, S, D, 0, k_new, v_new, n, p0);
 }
 
 /*

@@ -510,6 +510,32 @@ def check_append_ring(lib):
                     np.testing.assert_array_equal(vc[b, :, j], v[b, want[j]])
 
 
+def check_append_with_sinks(lib):
+    # Appending tokens 0..L-1 in pieces to a cache with pinned sinks reproduces the
+    # layout built directly (sink slots, then the ring of the last positions), and
+    # each written slot holds its token's rows.
+    B, Hkv, D, W, ns = 2, 2, 8, 8, 3
+    for L, pieces in [(2, [2]), (5, [1, 4]), (11, [11]), (30, [7, 7, 16]), (40, [40])]:
+        k = I.normal_bf16(150 + L, (B, L, Hkv, D))
+        v = I.normal_bf16(151 + L, (B, L, Hkv, D))
+        kc = I.normal_bf16(152, (B, Hkv, ns + W, D))
+        vc = I.normal_bf16(153, (B, Hkv, ns + W, D))
+        pos = np.full((B, ns + W), -1, dtype=np.int32)
+        p0 = 0
+        for n in pieces:
+            kc, vc, pos = oracle.cache_append(kc, vc, pos, k[:, p0:p0 + n], v[:, p0:p0 + n], [p0] * B, lib=lib,
+                                              n_sink=ns)
+            p0 += n
+        kref, vref, pref = _sink_cache(k, v, L, W, ns, ns + W, 152)
+        np.testing.assert_array_equal(pos, pref)
+        np.testing.assert_array_equal(pos, I.sink_ring_slot_positions(np.array([L] * B), W, ns))
+        for b in range(B):
+            for j in range(ns + W):
+                if pos[b, j] >= 0:
+                    np.testing.assert_array_equal(kc[b, :, j], k[b, pos[b, j]])
+                    np.testing.assert_array_equal(vc[b, :, j], v[b, pos[b, j]])
+
+
 def check_chunk_matches_prefill(lib):
     # Chunked prefill (history in the ring, chunk as new tokens) equals rows
     # p0 .. p0+C-1 of the causal-window prefill over the whole sequence.
@@ -578,5 +604,6 @@ ALL_CHECKS = [
     check_global_projection_identity,
     check_global_projection_roles,
     check_append_ring,
+    check_append_with_sinks,
     check_chunk_matches_prefill,
 ]

@@ -38,7 +38,9 @@ MUTATIONS = {
     "global-proj-query": ("(row_global ? qg : q)", "q"),
     "decode-sink-dropped": (" || p < n_sink", ""),
     "decode-sink-off-by-one": ("p < n_sink", "p <= n_sink"),
-    "append-slot-shift": ("const int64_t j = p % S;", "const int64_t j = (p + 1) % S;"),
+    "append-slot-shift": ("n_sink + (p - n_sink) % (S - n_sink);", "n_sink + (p + 1 - n_sink) % (S - n_sink);"),
+    "append-sinks-ignored": ("const int64_t j = p < n_sink ? p : n_sink + (p - n_sink) % (S - n_sink);",
+                             "const int64_t j = p % S;"),
     "append-order-reversed": ("const int64_t p = (int64_t)p0[b] + i;", "const int64_t p = (int64_t)p0[b] + (n - 1 - i);"),
     "chunk-history-overlap": ("if (p < p0[b] && slot_allowed", "if (slot_allowed"),
 }
