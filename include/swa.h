@@ -189,6 +189,84 @@ SWA_API size_t swa_decode_workspace_size(const swa_decode_params *p);
 SWA_API swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t workspace_bytes,
                       swa_stream_t stream);
 
+/*
+ * A ring-buffer KV cache (lizeman page, KV cache paragraph, after Mistral 7B section
+ * 2: the keys and values of token p are stored in slot p mod W, overwriting older
+ * ones).  A cache with n_sink pinned attention sinks keeps position p < n_sink in
+ * slot p and rings the other positions through the remaining slots:
+ *     slot(p) = p                                          if p < n_sink
+ *             = n_sink + (p - n_sink) mod (n_slots - n_sink) otherwise.
+ *   k_cache, v_cache  bf16 [B, H_kv, n_slots, d_h], contiguous
+ *   slot_pos          int32 [B, n_slots]: the position each slot holds (< 0: never written)
+ * This is the layout swa_decode reads (its W is n_slots).
+ */
+typedef struct swa_cache_params {
+    void *k_cache;
+    void *v_cache;
+    int32_t *slot_pos;
+    int32_t B, H_kv, d_h, n_slots, n_sink;
+} swa_cache_params;
+
+/*
+ * Appends n_new tokens to every sequence: token i of sequence b has position
+ * p0[b] + i and its rows k_new[b, i], v_new[b, i] (bf16 [B, n_new, H_kv, d_h],
+ * contiguous) go to slot(p) of every kv head, with slot_pos set to p.  Tokens are
+ * applied in order, so of two tokens mapping to one ring slot the later one stays.
+ * p0: device int32 [B], each >= 0 (a negative entry skips that sequence and is
+ * reported by swa_check_device_error as SWA_ERR_INVALID_ARG).
+ * Requirements: d_h in {64, 128, 256}; 0 <= n_sink < n_slots; pointers 16-byte
+ * aligned (slot_pos, p0: 4-byte).  n_new = 0 is a no-op.
+ */
+SWA_API swa_status swa_cache_append(const swa_cache_params *c, const void *k_new, const void *v_new, int32_t n_new,
+                            const int32_t *p0, swa_stream_t stream);
+
+/*
+ * Decode with the current token appended in the same pass: k_new, v_new (bf16
+ * [B, H_kv, d_h], contiguous) are written to slot(q_pos[b]) of p->k_cache and
+ * p->v_cache -- the slot rule of swa_cache_append with n_slots = p->W and n_sink =
+ * p->n_sink -- slot_pos there is set to q_pos[b], and the query attends exactly as
+ * swa_decode would after a separate swa_cache_append.  The caches and slot_pos are
+ * written: they must be writable device memory.  Workspace as swa_decode.
+ */
+SWA_API swa_status swa_decode_append(const swa_decode_params *p, const void *k_new, const void *v_new,
+                             void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
+/*
+ * Chunked prefill against a ring cache: C new tokens per sequence, at positions
+ * p0[b] .. p0[b] + C - 1, attend to the cached history and to the chunk itself; the
+ * query at position t keeps the keys at positions t - window < p <= t (lizeman page,
+ * section 2 window; the cache convention above).
+ *   q            bf16 [B, C, H_q, d_h], contiguous
+ *   k_new, v_new bf16 [B, C, H_kv, d_h], contiguous: the chunk's keys and values
+ *   p0           device int32 [B]: position of each sequence's first chunk token
+ *   o            bf16 [B, C, H_q, d_h]; lse fp32 [B, H_q, C]; row_counts optional [B, H_q, C]
+ *   append       nonzero: afterwards append the chunk to the cache (swa_cache_append)
+ * The cache must hold, for every sequence, every position in
+ * [max(0, p0 - n_slots), p0) -- the tokens appended before the chunk; a slot found
+ * holding another position is reported by swa_check_device_error as
+ * SWA_ERR_INVALID_ARG.  Requirements: the cache's B, H_kv, d_h match; n_sink = 0
+ * (a sink cache is SWA_ERR_UNSUPPORTED here); window >= 1; H_q / H_kv <= 16.
+ * Workspace: swa_prefill_chunk_workspace_size bytes, 256-byte aligned (the chunk's
+ * key/value rows and the window history gathered in position order).
+ */
+typedef struct swa_chunk_params {
+    const void *q;
+    const void *k_new;
+    const void *v_new;
+    const int32_t *p0;
+    int32_t B, C, H_q, H_kv, d_h;
+    int32_t window;
+    float scale;
+    void *o;
+    float *lse;
+    int32_t *row_counts;
+    int32_t append;
+} swa_chunk_params;
+
+SWA_API size_t swa_prefill_chunk_workspace_size(const swa_chunk_params *p, const swa_cache_params *c);
+SWA_API swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *c, void *workspace,
+                             size_t workspace_bytes, swa_stream_t stream);
+
 /* Bytes of the built-in scratch array used by swa_decode_noalloc (16 MiB per device). */
 #define SWA_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -216,7 +294,9 @@ SWA_API swa_status swa_decode_noalloc(const swa_decode_params *p, swa_stream_t s
 /*
  * Synchronises `stream`, then reads and clears the library's device error words.
  * Returns SWA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
- * call, SWA_ERR_CUDA if the synchronisation failed, else SWA_OK.
+ * call, SWA_ERR_INVALID_ARG if a kernel found device data breaking its contract
+ * (a negative append position, a cache slot not holding a position a chunked
+ * prefill needs), SWA_ERR_CUDA if the synchronisation failed, else SWA_OK.
  */
 SWA_API swa_status swa_check_device_error(swa_stream_t stream);
 

@@ -1,8 +1,9 @@
 """Sliding-window attention on GB300 (sm_103a): thin Python binding of libswa.so.
 
 The functions here marshal torch tensors into the C ABI of ``include/swa.h``
-(``swa_fwd``, ``swa_decode`` and their workspace queries) and call it on the
-current CUDA stream.  Every step of the computation runs in the library's
+(``swa_fwd``, ``swa_decode``, ``swa_cache_append``, ``swa_decode_append``,
+``swa_prefill_chunk`` and their workspace queries) and call it on the current
+CUDA stream.  Every step of the computation runs in the library's
 kernels; there is no fallback path.  If the library has not been built, the
 first call raises (``build()`` compiles it in-tree with nvcc).
 
@@ -20,6 +21,7 @@ __all__ = [
     "swa_fwd", "swa_decode", "swa_fwd_workspace_size", "swa_decode_workspace_size",
     "swa_check_device_error", "swa_status_string", "swa_abi_version",
     "SwaFwdParams", "SwaDecodeParams", "GLOBAL_FULL", "GLOBAL_SINK",
+    "SwaCacheParams", "SwaChunkParams", "swa_cache_append", "swa_decode_append", "swa_prefill_chunk",
 ]
 
 _c_i64x3 = ctypes.c_int64 * 3
@@ -51,6 +53,27 @@ class SwaDecodeParams(ctypes.Structure):
         ("W", ctypes.c_int32), ("scale", ctypes.c_float),
         ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p),
         ("window", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+    ]
+
+
+class SwaCacheParams(ctypes.Structure):
+    """Mirror of ``swa_cache_params`` in include/swa.h."""
+
+    _fields_ = [
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p),
+        ("B", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d_h", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+        ("n_sink", ctypes.c_int32),
+    ]
+
+
+class SwaChunkParams(ctypes.Structure):
+    """Mirror of ``swa_chunk_params`` in include/swa.h."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("p0", ctypes.c_void_p),
+        ("B", ctypes.c_int32), ("C", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32),
+        ("d_h", ctypes.c_int32), ("window", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p), ("append", ctypes.c_int32),
     ]
 
 
@@ -102,6 +125,14 @@ def load_library(path: str | None = None):
     lib.swa_decode.restype = ctypes.c_int
     lib.swa_decode_noalloc.argtypes = [ctypes.POINTER(SwaDecodeParams), vp]
     lib.swa_decode_noalloc.restype = ctypes.c_int
+    lib.swa_cache_append.argtypes = [ctypes.POINTER(SwaCacheParams), vp, vp, ctypes.c_int32, vp, vp]
+    lib.swa_cache_append.restype = ctypes.c_int
+    lib.swa_decode_append.argtypes = [ctypes.POINTER(SwaDecodeParams), vp, vp, vp, sz, vp]
+    lib.swa_decode_append.restype = ctypes.c_int
+    lib.swa_prefill_chunk_workspace_size.argtypes = [ctypes.POINTER(SwaChunkParams), ctypes.POINTER(SwaCacheParams)]
+    lib.swa_prefill_chunk_workspace_size.restype = sz
+    lib.swa_prefill_chunk.argtypes = [ctypes.POINTER(SwaChunkParams), ctypes.POINTER(SwaCacheParams), vp, sz, vp]
+    lib.swa_prefill_chunk.restype = ctypes.c_int
     lib.swa_check_device_error.argtypes = [vp]
     lib.swa_check_device_error.restype = ctypes.c_int
     lib.swa_last_error_string.argtypes = []
@@ -286,6 +317,124 @@ def swa_decode(q, k_cache, v_cache, slot_pos, q_pos, scale: float | None = None,
     st = lib.swa_decode(ctypes.byref(p), _ptr(workspace), ws_bytes, _stream_handle(stream))
     if st != 0:
         raise SwaError("swa_decode", st)
+    return o, lse, row_counts
+
+
+def cache_params(k_cache, v_cache, slot_pos, n_sink: int = 0) -> SwaCacheParams:
+    """caches bf16 [B,H_kv,n_slots,d] and slot_pos int32 [B,n_slots] (contiguous, CUDA)."""
+    c = SwaCacheParams()
+    c.k_cache, c.v_cache, c.slot_pos = k_cache.data_ptr(), v_cache.data_ptr(), slot_pos.data_ptr()
+    c.B, c.H_kv, c.n_slots, c.d_h = k_cache.shape
+    c.n_sink = int(n_sink)
+    return c
+
+
+def _check_cache(k_cache, v_cache, slot_pos):
+    import torch
+
+    _check_bf16("k_cache", k_cache, 4)
+    _check_bf16("v_cache", v_cache, 4)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("slot_pos", slot_pos)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+    if slot_pos.dtype != torch.int32 or v_cache.shape != k_cache.shape or tuple(slot_pos.shape) != tuple(k_cache.shape[::2]):
+        raise ValueError("slot_pos: expected int32 [B, n_slots] matching the caches")
+
+
+def swa_cache_append(k_cache, v_cache, slot_pos, k_new, v_new, p0, *, n_sink: int = 0, stream=None) -> None:
+    """Append k_new/v_new [B,n,H_kv,d] (positions p0[b] + i, p0 int32 CUDA [B]) to the
+    ring cache in place (slot rule of include/swa.h with n_sink pinned sinks)."""
+    import torch
+
+    _check_cache(k_cache, v_cache, slot_pos)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _check_bf16(name, t, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+    if p0.dtype != torch.int32 or not p0.is_contiguous():
+        raise ValueError("p0: expected a contiguous int32 tensor")
+    c = cache_params(k_cache, v_cache, slot_pos, n_sink)
+    st = load_library().swa_cache_append(ctypes.byref(c), _ptr(k_new), _ptr(v_new), int(k_new.shape[1]), _ptr(p0),
+                                         _stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_cache_append", st)
+
+
+def swa_decode_append(q, k_cache, v_cache, slot_pos, q_pos, k_new, v_new, scale: float | None = None, *, o=None,
+                      lse=None, want_counts: bool = False, workspace=None, stream=None, window: int = 0,
+                      n_sink: int = 0):
+    """swa_decode with the current token's k_new/v_new [B,H_kv,d] appended to the cache
+    (in place) in the same pass.  Returns (o, lse, row_counts or None)."""
+    import torch
+
+    lib = load_library()
+    _check_bf16("q", q, 3)
+    _check_cache(k_cache, v_cache, slot_pos)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _check_bf16(name, t, 3)
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    row_counts = torch.empty((B, Hq), dtype=torch.int32, device=q.device) if want_counts else None
+    p = decode_params(q, k_cache, v_cache, slot_pos, q_pos, scale, o, lse, row_counts, window, n_sink)
+    need = int(lib.swa_decode_workspace_size(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.swa_decode_append(ctypes.byref(p), _ptr(k_new), _ptr(v_new), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_decode_append", st)
+    return o, lse, row_counts
+
+
+def chunk_params(q, k_new, v_new, p0, window: int, scale: float, o, lse, row_counts, append: bool) -> SwaChunkParams:
+    B, C, Hq, D = q.shape
+    p = SwaChunkParams()
+    p.q, p.k_new, p.v_new, p.p0 = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), p0.data_ptr()
+    p.B, p.C, p.H_q, p.H_kv, p.d_h = B, C, Hq, k_new.shape[2], D
+    p.window, p.scale = int(window), float(scale)
+    p.o, p.lse = o.data_ptr(), lse.data_ptr()
+    p.row_counts = None if row_counts is None else row_counts.data_ptr()
+    p.append = 1 if append else 0
+    return p
+
+
+def swa_prefill_chunk(q, k_new, v_new, k_cache, v_cache, slot_pos, p0, window: int, scale: float | None = None, *,
+                      append: bool = False, o=None, lse=None, want_counts: bool = False, workspace=None,
+                      stream=None):
+    """Chunked prefill: q [B,C,H_q,d] and the chunk's k_new/v_new [B,C,H_kv,d] at positions
+    p0[b] + i attend to the ring cache's history and to the chunk (causal window).
+    append: afterwards the chunk joins the cache.  Returns (o [B,C,H_q,d], lse [B,H_q,C],
+    row_counts or None)."""
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new)):
+        _check_bf16(name, t, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+    _check_cache(k_cache, v_cache, slot_pos)
+    if p0.dtype != torch.int32 or not p0.is_contiguous():
+        raise ValueError("p0: expected a contiguous int32 tensor")
+    B, C, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, C), dtype=torch.float32, device=q.device) if lse is None else lse
+    row_counts = torch.empty((B, Hq, C), dtype=torch.int32, device=q.device) if want_counts else None
+    p = chunk_params(q, k_new, v_new, p0, window, scale, o, lse, row_counts, append)
+    c = cache_params(k_cache, v_cache, slot_pos)
+    need = int(lib.swa_prefill_chunk_workspace_size(ctypes.byref(p), ctypes.byref(c)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.swa_prefill_chunk(ctypes.byref(p), ctypes.byref(c), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != 0:
+        raise SwaError("swa_prefill_chunk", st)
     return o, lse, row_counts
 
 

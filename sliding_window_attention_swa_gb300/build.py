@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libswa.so")
-SOURCES = ["swa_abi.cu", "swa_band.cu", "swa_split.cu", "swa_noalloc.cu"]
+SOURCES = ["swa_abi.cu", "swa_band.cu", "swa_split.cu", "swa_noalloc.cu", "swa_cache.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

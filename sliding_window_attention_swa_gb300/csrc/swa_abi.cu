@@ -81,6 +81,64 @@ swa_status decode_check(const swa_decode_params *p) {
     return SWA_OK;
 }
 
+swa_status cache_check(const swa_cache_params *c) {
+    if (!c || !c->k_cache || !c->v_cache || !c->slot_pos) return SWA_ERR_INVALID_ARG;
+    if (c->B < 1 || c->H_kv < 1 || c->d_h < 1 || c->n_slots < 1) return SWA_ERR_INVALID_ARG;
+    if (c->n_sink < 0 || c->n_sink >= c->n_slots) return SWA_ERR_INVALID_ARG;
+    if (!head_dim_ok(c->d_h)) return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_cache) || !aligned16(c->v_cache) || (reinterpret_cast<uintptr_t>(c->slot_pos) & 3u))
+        return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+swa_status chunk_check(const swa_chunk_params *p, const swa_cache_params *c) {
+    swa_status st = cache_check(c);
+    if (st != SWA_OK) return st;
+    if (!p || !p->q || !p->k_new || !p->v_new || !p->p0 || !p->o || !p->lse) return SWA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->C < 1 || p->H_q < 1 || p->H_kv < 1 || p->d_h < 1 || p->window < 1) return SWA_ERR_INVALID_ARG;
+    if (p->H_q % p->H_kv != 0 || p->B != c->B || p->H_kv != c->H_kv || p->d_h != c->d_h) return SWA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(p->window) - 1 + p->C > (1 << 30)) return SWA_ERR_INVALID_ARG;
+    if (c->n_sink != 0) return SWA_ERR_UNSUPPORTED;
+    if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
+    if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
+    if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(p->q) || !aligned16(p->k_new) || !aligned16(p->v_new) || !aligned16(p->o) ||
+        (reinterpret_cast<uintptr_t>(p->p0) & 3u) || (reinterpret_cast<uintptr_t>(p->lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(p->row_counts) & 3u))
+        return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+// Workspace of a chunked prefill: gathered keys, gathered values, kmin.
+struct ChunkWs {
+    size_t kv_bytes, total;
+};
+ChunkWs chunk_ws(const swa_chunk_params *p) {
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t rows = static_cast<size_t>(p->B) * (static_cast<size_t>(p->window) - 1 + p->C) * p->H_kv;
+    const size_t kv = up(rows * p->d_h * 2);
+    return {kv, 2 * kv + up(static_cast<size_t>(p->B) * 4)};
+}
+
+swa::AppendArgs append_args(const swa_cache_params *c, const void *k_new, const void *v_new, int n,
+                            const int32_t *p0) {
+    swa::AppendArgs a{};
+    a.kc = static_cast<uint16_t *>(c->k_cache);
+    a.vc = static_cast<uint16_t *>(c->v_cache);
+    a.slot_pos = c->slot_pos;
+    a.B = c->B;
+    a.H_kv = c->H_kv;
+    a.D = c->d_h;
+    a.n_slots = c->n_slots;
+    a.n_sink = c->n_sink;
+    a.kn = static_cast<const uint16_t *>(k_new);
+    a.vn = static_cast<const uint16_t *>(v_new);
+    a.n = n;
+    a.p0 = p0;
+    return a;
+}
+
 swa_status workspace_ok(void *ws, size_t have, size_t need) {
     if (need == 0) return SWA_OK;
     if (!ws || have < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SWA_ERR_WORKSPACE;
@@ -164,7 +222,8 @@ size_t swa::decode_workspace_bytes(const swa_decode_params *p) {
     return split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, p->W);
 }
 
-cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s) {
+cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s, const void *k_new,
+                            const void *v_new) {
     const int64_t D = p->d_h, W = p->W;
     SplitArgs sa{};
     sa.q = p->q;
@@ -193,6 +252,9 @@ cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s
     sa.n_splits = split_count(p->W);
     sa.q_per_cta = split_q_per_cta(p->H_q / p->H_kv);
     split_carve(ws, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
+    sa.k_new = static_cast<const uint16_t *>(k_new);
+    sa.v_new = static_cast<const uint16_t *>(v_new);
+    sa.slot_pos_w = const_cast<int32_t *>(p->slot_pos);
     cudaError_t e = launch_split(sa, s);
     if (e != cudaSuccess) return e;
 
@@ -372,10 +434,115 @@ swa_status swa_decode(const swa_decode_params *p, void *workspace, size_t worksp
     return SWA_OK;
 }
 
+swa_status swa_cache_append(const swa_cache_params *c, const void *k_new, const void *v_new, int32_t n_new,
+                            const int32_t *p0, swa_stream_t stream) {
+    swa_status st = cache_check(c);
+    if (st != SWA_OK) return st;
+    if (n_new < 0 || (n_new > 0 && (!k_new || !v_new || !p0))) return SWA_ERR_INVALID_ARG;
+    if (n_new == 0) return SWA_OK;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(p0) & 3u)) return SWA_ERR_UNSUPPORTED;
+    if (failed(swa::launch_append(append_args(c, k_new, v_new, n_new, p0), reinterpret_cast<cudaStream_t>(stream))))
+        return SWA_ERR_CUDA;
+    return SWA_OK;
+}
+
+swa_status swa_decode_append(const swa_decode_params *p, const void *k_new, const void *v_new, void *workspace,
+                             size_t workspace_bytes, swa_stream_t stream) {
+    swa_status st = decode_check(p);
+    if (st != SWA_OK) return st;
+    if (!k_new || !v_new || p->n_sink >= p->W) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return SWA_ERR_UNSUPPORTED;
+    st = workspace_ok(workspace, workspace_bytes, swa_decode_workspace_size(p));
+    if (st != SWA_OK) return st;
+    if (failed(swa::run_decode(p, workspace, reinterpret_cast<cudaStream_t>(stream), k_new, v_new)))
+        return SWA_ERR_CUDA;
+    return SWA_OK;
+}
+
+size_t swa_prefill_chunk_workspace_size(const swa_chunk_params *p, const swa_cache_params *c) {
+    if (chunk_check(p, c) != SWA_OK) return 0;
+    return chunk_ws(p).total;
+}
+
+swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *c, void *workspace,
+                             size_t workspace_bytes, swa_stream_t stream) {
+    swa_status st = chunk_check(p, c);
+    if (st != SWA_OK) return st;
+    const ChunkWs ws = chunk_ws(p);
+    st = workspace_ok(workspace, workspace_bytes, ws.total);
+    if (st != SWA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int W = p->window, C = p->C, Tk = W - 1 + C;
+    char *w = static_cast<char *>(workspace);
+    uint16_t *kl = reinterpret_cast<uint16_t *>(w);
+    uint16_t *vl = reinterpret_cast<uint16_t *>(w + ws.kv_bytes);
+    int32_t *kmin = reinterpret_cast<int32_t *>(w + 2 * ws.kv_bytes);
+
+    // 1. the window history (positions p0-W+1 .. p0-1) in position order, then the chunk
+    swa::GatherArgs ga{};
+    ga.kc = static_cast<const uint16_t *>(c->k_cache);
+    ga.vc = static_cast<const uint16_t *>(c->v_cache);
+    ga.slot_pos = c->slot_pos;
+    ga.B = p->B;
+    ga.H_kv = p->H_kv;
+    ga.D = p->d_h;
+    ga.n_slots = c->n_slots;
+    ga.kn = static_cast<const uint16_t *>(p->k_new);
+    ga.vn = static_cast<const uint16_t *>(p->v_new);
+    ga.C = C;
+    ga.W = W;
+    ga.p0 = p->p0;
+    ga.kl = kl;
+    ga.vl = vl;
+    ga.kmin = kmin;
+    if (failed(swa::launch_gather(ga, s))) return SWA_ERR_CUDA;
+
+    // 2. the causal window over that key sequence: query i sits at key index W-1+i
+    const int64_t D = p->d_h;
+    swa::BandArgs ba{};
+    ba.q = p->q;
+    ba.k = kl;
+    ba.v = vl;
+    ba.o = p->o;
+    const int64_t qs[3] = {static_cast<int64_t>(C) * p->H_q * D, p->H_q * D, D};
+    const int64_t ks[3] = {static_cast<int64_t>(Tk) * p->H_kv * D, p->H_kv * D, D};
+    for (int i = 0; i < 3; ++i) {
+        ba.q_st[i] = ba.o_st[i] = qs[i];
+        ba.k_st[i] = ba.v_st[i] = ba.kg_st[i] = ba.vg_st[i] = ks[i];
+    }
+    ba.B = p->B;
+    ba.T = C;
+    ba.Tk = Tk;
+    ba.q_off = W - 1;
+    ba.kmin = kmin;
+    ba.H_q = p->H_q;
+    ba.H_kv = p->H_kv;
+    ba.D = p->d_h;
+    ba.wl = W - 1;
+    ba.wr = 0;
+    ba.scale_log2 = p->scale * kLog2e;
+    ba.kg = kl;
+    ba.vg = vl;
+    ba.lse = p->lse;
+    ba.counts = p->row_counts;
+    ba.lse_st[0] = static_cast<int64_t>(p->H_q) * C;
+    ba.lse_st[1] = C;
+    ba.lse_st[2] = 1;
+    if (failed(swa::launch_band(ba, s))) return SWA_ERR_CUDA;
+
+    // 3. the chunk joins the cache
+    if (p->append &&
+        failed(swa::launch_append(append_args(c, p->k_new, p->v_new, C, p->p0), s)))
+        return SWA_ERR_CUDA;
+    return SWA_OK;
+}
+
 swa_status swa_check_device_error(swa_stream_t stream) {
     if (failed(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)))) return SWA_ERR_CUDA;
     const unsigned int e = swa::band_read_clear_error() | swa::split_read_clear_error();
-    return e ? SWA_ERR_TIMEOUT : SWA_OK;
+    const unsigned int c = swa::cache_read_clear_error();
+    if (e) return SWA_ERR_TIMEOUT;
+    return c ? SWA_ERR_INVALID_ARG : SWA_OK;
 }
 
 }  // extern "C"

@@ -88,6 +88,10 @@ struct BandCfg {
 
 struct BandKernelArgs {
     int B, T, H_q, H_kv, G, TQ, n_units_t, n_units;
+    // Keys live in their own index space of Tk positions: query row t sits at key
+    // index t + q_off, and keys below kmin[b] (when kmin is set) do not exist.
+    int Tk, q_off;
+    const int32_t *kmin;
     int wl, wr;
     float scale_log2;
     const int32_t *global_idx;
@@ -129,7 +133,7 @@ __device__ __forceinline__ bool global_bits(const int32_t *g, int n, int k0, uin
 
 // Geometry of work unit u (units are numbered longest first).
 struct Unit {
-    int b, kvh, t0, kv_lo, n_band, n_tiles;
+    int b, kvh, t0, kv_lo, n_band, n_tiles, kmin;
 };
 
 template <int NQT, int BN>
@@ -141,8 +145,9 @@ __device__ __forceinline__ Unit unit_of(int u, const BandKernelArgs &a) {
     w.kvh = bh % a.H_kv;
     w.t0 = ut * NQT * a.TQ;
     const int t1 = min(a.T - 1, w.t0 + NQT * a.TQ - 1);
-    w.kv_lo = a.wl < 0 ? 0 : max(0, w.t0 - a.wl);
-    const int kv_hi = a.wr < 0 ? a.T - 1 : min(a.T - 1, t1 + a.wr);
+    w.kmin = a.kmin ? __ldg(a.kmin + w.b) : 0;
+    w.kv_lo = a.wl < 0 ? w.kmin : max(w.kmin, w.t0 + a.q_off - a.wl);
+    const int kv_hi = a.wr < 0 ? a.Tk - 1 : min(a.Tk - 1, t1 + a.q_off + a.wr);
     w.n_band = (kv_hi - w.kv_lo + BN) / BN;
     w.n_tiles = w.n_band + (a.n_global + BN - 1) / BN;
     return w;
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         int srow = -1;
                         if (gi < a.n_global) {
                             const int gs = a.global_idx[gi];
-                            if (gs >= 0 && gs < a.T) srow = gs;
+                            if (gs >= 0 && gs < a.Tk) srow = gs;
                         }
                         uint4 val = make_uint4(0, 0, 0, 0);
                         if (srow >= 0)
@@ -442,10 +447,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             const int t = tx + tq;
             const bool row_ok = tq < a.TQ && t < a.T;
             const int h = w.kvh * a.G + hj;
-            const int tlo = tx, thi = min(a.T - 1, tx + a.TQ - 1);
-            // this row's band, clipped to [0, T)
-            const int lo_abs = a.wl < 0 ? 0 : max(0, t - a.wl);
-            const int hi_abs = a.wr < 0 ? a.T - 1 : min(a.T - 1, t + a.wr);
+            // key-index positions of this tile's first and last rows and of this row
+            const int tlo = tx + a.q_off, thi = min(a.T - 1, tx + a.TQ - 1) + a.q_off;
+            const int tk = t + a.q_off;
+            // this row's band, clipped to [kmin, Tk)
+            const int lo_abs = a.wl < 0 ? w.kmin : max(w.kmin, tk - a.wl);
+            const int hi_abs = a.wr < 0 ? a.Tk - 1 : min(a.Tk - 1, tk + a.wr);
             float m = -INFINITY, l = 0.f;
             int count = 0;
 #pragma unroll 1
@@ -474,7 +481,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (j < w.n_band) {
                     const int k0 = w.kv_lo + j * BN;
                     const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
-                                          (k0 + BN - 1 <= a.T - 1);
+                                          (k0 + BN - 1 <= a.Tk - 1);
                     if (interior) {
                         count += BN;
                     } else {
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         // kept: outside the row's band (sinks: left of it); with separate
                         // projections every global key is scored here
                         const bool outside = (gs < lo_abs) | ((gs > hi_abs) & !a.sink);
-                        const bool al = (gs >= 0) & (gs < a.T) & (outside | (a.sep != 0));
+                        const bool al = (gs >= 0) & (gs < a.Tk) & (outside | (a.sep != 0));
                         cnt4[c & 3] += al ? 1 : 0;
                         x[c] = al ? x[c] : -INFINITY;
                     }
@@ -704,13 +711,17 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     const int G = x.H_q / x.H_kv;
     const int TQ = BM / G;
     CUtensorMap mq, mk, mv;
+    const int Tk = x.Tk > 0 ? x.Tk : x.T;
     if (!make_map(&mq, x.q, D, x.H_q, x.T, x.B, x.q_st, G, TQ) ||
-        !make_map(&mk, x.k, D, x.H_kv, x.T, x.B, x.k_st, 1, C::BN) ||
-        !make_map(&mv, x.v, D, x.H_kv, x.T, x.B, x.v_st, 1, C::BN))
+        !make_map(&mk, x.k, D, x.H_kv, Tk, x.B, x.k_st, 1, C::BN) ||
+        !make_map(&mv, x.v, D, x.H_kv, Tk, x.B, x.v_st, 1, C::BN))
         return cudaErrorInvalidValue;
     BandKernelArgs a{};
     a.B = x.B;
     a.T = x.T;
+    a.Tk = Tk;
+    a.q_off = x.q_off;
+    a.kmin = x.kmin;
     a.H_q = x.H_q;
     a.H_kv = x.H_kv;
     a.G = G;

@@ -36,6 +36,10 @@ struct SplitArgs {
     float *ws_ml;     // [B, NQ, H_q, n_splits, 2]   (max in log2 units, sum)
     float *ws_acc;    // [B, NQ, H_q, n_splits, D]   unnormalised weighted values
     int32_t *ws_cnt;  // [B, H_kv, n_splits]         valid slots per split
+    // Decode only: the current token's key/value rows [B, H_kv, D] to write into slot
+    // slot(q_pos[b]) before it is read (nullptr: none), and slot_pos to update there.
+    const uint16_t *k_new, *v_new;
+    int32_t *slot_pos_w;
 };
 
 struct MergeArgs {
@@ -101,15 +105,48 @@ struct BandArgs {
     float *lse;
     int32_t *counts;
     int64_t lse_st[3];  // element strides (b, h, t) of lse and counts
+    // Keys in their own index space (chunked prefill): Tk key rows (0: T), query row t
+    // at key index t + q_off, keys below kmin[b] absent (kmin: device [B] or nullptr).
+    int Tk, q_off;
+    const int32_t *kmin;
 };
 cudaError_t launch_band(const BandArgs &a, cudaStream_t s);
+
+// Ring-buffer cache (swa_cache.cu).  Slot rule: p < n_sink -> p, else
+// n_sink + (p - n_sink) mod (n_slots - n_sink).
+struct AppendArgs {
+    uint16_t *kc, *vc;     // [B, H_kv, n_slots, D] bf16 bits
+    int32_t *slot_pos;     // [B, n_slots]
+    int B, H_kv, D, n_slots, n_sink;
+    const uint16_t *kn, *vn;  // [B, n, H_kv, D]
+    int n;
+    const int32_t *p0;     // [B] position of token 0
+};
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
+
+// Window history of a chunk in position order, then the chunk: kl/vl [B, W-1+C, H_kv, D]
+// and kmin[b], the first key index present (ring without sinks: slot p mod n_slots).
+struct GatherArgs {
+    const uint16_t *kc, *vc;
+    const int32_t *slot_pos;
+    int B, H_kv, D, n_slots;
+    const uint16_t *kn, *vn;  // [B, C, H_kv, D]
+    int C, W;
+    const int32_t *p0;
+    uint16_t *kl, *vl;
+    int32_t *kmin;
+};
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
+unsigned int cache_read_clear_error();  // bit 0: bad position, bit 1: cache mismatch
 
 // Host-side helpers of the C ABI shared with the allocation-free decode entry point.
 swa_status validate_decode(const swa_decode_params *p);  // the checks swa_decode applies
 // Bytes of split partials a decode of `p` needs, and the split + merge launches of a
 // validated decode into workspace `ws` (at least that many bytes, 256-byte aligned).
 size_t decode_workspace_bytes(const swa_decode_params *p);
-cudaError_t run_decode(const swa_decode_params *p, void *ws, cudaStream_t s);
+// k_new / v_new (bf16 [B, H_kv, d_h]) non-null: the current token is appended first.
+cudaError_t run_decode(const swa_decode_params *p, void *ws, cudaStream_t s, const void *k_new = nullptr,
+                       const void *v_new = nullptr);
 bool record_cuda_failure(cudaError_t e);                  // true (and recorded) if e failed
 unsigned int band_read_clear_error();
 

@@ -155,6 +155,15 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
             const int kvh = y / ka.nqb, qb = y % ka.nqb;
             const int slot0 = split * a.slots_per_split;
             const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[b]) : 0;
+            // decode with append: the current token goes to slot(t) before it is read;
+            // si_new is that slot's index in this split (-1: not in this split)
+            int si_new = -1, s_new = 0;
+            if (a.k_new && t >= 0) {
+                s_new = t < a.n_sink ? static_cast<int>(t)
+                                     : a.n_sink + static_cast<int>((t - a.n_sink) % (a.n_slots - a.n_sink));
+                const int rel = s_new - slot0;
+                if (rel >= 0 && rel < a.slots_per_split && s_new < a.n_slots) si_new = rel;
+            }
             load_pos(item + gridDim.x, pos_next);
             // validity of the item's slots, 64 per chunk (two ballots)
             bool v[2 * MAX_CHUNKS];
@@ -163,6 +172,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 const int64_t p = pos_cur[i];
                 v[i] = pos_cur[i] != INT_MIN &&
                        (!a.slot_pos || (p >= 0 && p <= t && (p > t - a.W || p < a.n_sink)));
+                v[i] = v[i] || (i * 32 + lane == si_new);  // the appended token, position t
             }
             unsigned long long mask[MAX_CHUNKS];
             int count = 0;
@@ -177,6 +187,8 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
             for (int i = 0; i < 2 * MAX_CHUNKS; ++i) pos_cur[i] = pos_next[i];
             if (qb == 0 && lane == 0)
                 a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_splits + split] = count;
+            if (si_new >= 0 && kvh == 0 && qb == 0 && lane == 0)
+                a.slot_pos_w[static_cast<int64_t>(b) * a.n_slots + s_new] = static_cast<int32_t>(t);
             int last_c = -1;
 #pragma unroll
             for (int c = 0; c < MAX_CHUNKS; ++c)
@@ -190,6 +202,22 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 if (seq >= NST) {
                     ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
                     if (!ok) break;
+                }
+                if (si_new >= 0 && c == si_new / CH) {
+                    // write the current token's key and value rows into its slot, then make
+                    // those generic-proxy stores visible to the TMA load of this chunk
+                    const uint4 *ks = reinterpret_cast<const uint4 *>(a.k_new + (static_cast<int64_t>(b) * a.H_kv + kvh) * D);
+                    const uint4 *vs = reinterpret_cast<const uint4 *>(a.v_new + (static_cast<int64_t>(b) * a.H_kv + kvh) * D);
+                    uint4 *kd = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(a.k)) +
+                                                          b * a.k_sb + static_cast<int64_t>(s_new) * a.k_ss + kvh * a.k_sh);
+                    uint4 *vd = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(a.v)) +
+                                                          b * a.v_sb + static_cast<int64_t>(s_new) * a.v_ss + kvh * a.v_sh);
+                    for (int pc = lane; pc < 2 * (D / 8); pc += 32) {
+                        if (pc < D / 8) kd[pc] = __ldg(ks + pc);
+                        else vd[pc - D / 8] = __ldg(vs + pc - D / 8);
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __syncwarp();
                 }
                 if (lane == 0) {
                     StageHdr &h = hdr[st];

@@ -42,7 +42,8 @@ def test_version_and_status_strings(lib):
 
 def test_struct_layout_matches_header(tmp_path):
     # The C compiler's sizeof / offsetof of every field against the ctypes mirrors.
-    structs = {"swa_fwd_params": swa.SwaFwdParams, "swa_decode_params": swa.SwaDecodeParams}
+    structs = {"swa_fwd_params": swa.SwaFwdParams, "swa_decode_params": swa.SwaDecodeParams,
+               "swa_cache_params": swa.SwaCacheParams, "swa_chunk_params": swa.SwaChunkParams}
     lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "swa.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -144,6 +145,75 @@ def test_decode_workspace(lib):
     need = lib.swa_decode_workspace_size(ctypes.byref(p))
     assert need > 0
     assert lib.swa_decode(ctypes.byref(p), None, 0, None) == 5
+
+
+def _valid_cache():
+    c = swa.SwaCacheParams()
+    c.k_cache = c.v_cache = c.slot_pos = 0x10000
+    c.B, c.H_kv, c.d_h, c.n_slots, c.n_sink = 2, 2, 128, 256, 0
+    return c
+
+
+def _valid_chunk():
+    p = swa.SwaChunkParams()
+    p.q = p.k_new = p.v_new = p.p0 = p.o = p.lse = 0x10000
+    p.B, p.C, p.H_q, p.H_kv, p.d_h = 2, 64, 8, 2, 128
+    p.window, p.scale = 128, 0.1
+    return p
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda c: setattr(c, "slot_pos", None), 1),
+    (lambda c: setattr(c, "n_slots", 0), 1),
+    (lambda c: setattr(c, "n_sink", 256), 1),      # no ring slot left
+    (lambda c: setattr(c, "d_h", 96), 2),
+    (lambda c: setattr(c, "k_cache", 0x10008), 2),
+])
+def test_cache_append_rejects(lib, mutate, status):
+    c = _valid_cache()
+    mutate(c)
+    assert lib.swa_cache_append(ctypes.byref(c), 0x20000, 0x20000, 4, 0x30000, None) == status
+
+
+def test_cache_append_arguments(lib):
+    c = _valid_cache()
+    assert lib.swa_cache_append(ctypes.byref(c), None, None, 0, None, None) == 0  # nothing to append
+    assert lib.swa_cache_append(ctypes.byref(c), None, 0x20000, 4, 0x30000, None) == 1
+    assert lib.swa_cache_append(ctypes.byref(c), 0x20000, 0x20000, -1, 0x30000, None) == 1
+    assert lib.swa_cache_append(ctypes.byref(c), 0x20008, 0x20000, 4, 0x30000, None) == 2
+
+
+def test_decode_append_rejects(lib):
+    p = _valid_decode()
+    assert lib.swa_decode_append(ctypes.byref(p), None, 0x20000, None, 0, None) == 1
+    p.n_sink = p.W
+    assert lib.swa_decode_append(ctypes.byref(p), 0x20000, 0x20000, None, 0, None) == 1
+    p.n_sink = 0
+    assert lib.swa_decode_append(ctypes.byref(p), 0x20000, 0x20000, None, 0, None) == 5  # workspace
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p, c: setattr(p, "p0", None), 1),
+    (lambda p, c: setattr(p, "window", 0), 1),
+    (lambda p, c: setattr(p, "C", 0), 1),
+    (lambda p, c: setattr(p, "B", 3), 1),           # cache of 2 sequences
+    (lambda p, c: setattr(p, "d_h", 64), 1),        # cache head dim 128
+    (lambda p, c: setattr(c, "n_sink", 4), 2),      # sink caches not taken here
+    (lambda p, c: setattr(p, "q", 0x10004), 2),
+])
+def test_prefill_chunk_rejects(lib, mutate, status):
+    p, c = _valid_chunk(), _valid_cache()
+    mutate(p, c)
+    assert lib.swa_prefill_chunk(ctypes.byref(p), ctypes.byref(c), None, 0, None) == status
+    assert lib.swa_prefill_chunk_workspace_size(ctypes.byref(p), ctypes.byref(c)) == 0
+
+
+def test_prefill_chunk_workspace(lib):
+    p, c = _valid_chunk(), _valid_cache()
+    need = lib.swa_prefill_chunk_workspace_size(ctypes.byref(p), ctypes.byref(c))
+    # gathered keys and values: B * (W - 1 + C) * H_kv * d_h bf16 each, plus kmin
+    assert need >= 2 * 2 * (128 - 1 + 64) * 2 * 128 * 2
+    assert lib.swa_prefill_chunk(ctypes.byref(p), ctypes.byref(c), None, 0, None) == 5
 
 
 def test_missing_library_fails_loudly(tmp_path):
