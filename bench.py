@@ -281,6 +281,91 @@ def measure_decode(cfg, steps, warmup, device, flush, n_sink: int = 0):
     return {"ms": ms, "flops": flops, "bytes": nbytes, "launches_per_step": 2}
 
 
+def measure_cache_paths(steps, warmup, device, flush):
+    """The ring-buffer cache paths on the decode and Mistral shapes:
+    * chunked prefill: the last 4096 tokens of the Mistral-shape sequence as one chunk
+      against a 4096-slot ring holding the 4096 tokens before it (gather + band kernel);
+    * append: 512 new tokens for each of the 64 decode sequences (after their lengths);
+    * decode with the current token appended in the same pass (decode workload)."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    out = {}
+    stream = torch.cuda.current_stream()
+    # chunked prefill
+    cfg = I.MISTRAL
+    W, C = cfg.window_left + 1, 4096
+    p0 = cfg.T - C
+    q, k, v = I.prefill_inputs(cfg)
+    qc = to_dev(q[:, p0:], device)
+    kn, vn = to_dev(k[:, p0:], device), to_dev(v[:, p0:], device)
+    kh, vh = to_dev(k[:, p0 - W:p0], device), to_dev(v[:, p0 - W:p0], device)
+    del q, k, v
+    kc = torch.empty((1, cfg.Hkv, W, cfg.d), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    pos = torch.full((1, W), -1, dtype=torch.int32, device=device)
+    swa.swa_cache_append(kc, vc, pos, kh, vh, torch.tensor([p0 - W], dtype=torch.int32, device=device))
+    p0d = torch.tensor([p0], dtype=torch.int32, device=device)
+    o = torch.empty_like(qc)
+    lse = torch.empty((1, cfg.Hq, C), dtype=torch.float32, device=device)
+    pc = swa.chunk_params(qc, kn, vn, p0d, W, cfg.scale, o, lse, None, False)
+    cc = swa.cache_params(kc, vc, pos)
+    ws = torch.empty(int(swa.load_library().swa_prefill_chunk_workspace_size(pc, cc)), dtype=torch.uint8,
+                     device=device)
+
+    def chunk():
+        swa.swa_prefill_chunk(qc, kn, vn, kc, vc, pos, p0d, W, cfg.scale, o=o, lse=lse, workspace=ws, stream=stream)
+
+    ms = timed_steps(chunk, steps, warmup, flush, stream)
+    swa.swa_check_device_error()
+    flops = 4.0 * cfg.d * C * W * cfg.Hq
+    out["chunked_prefill"] = {"ms": ms, "flops": flops, "launches_per_step": 2,
+                              "workload": f"{cfg.name}: chunk of {C} tokens at position {p0}, {W}-slot ring"}
+    del qc, kn, vn, kh, vh, kc, vc, pos, o, lse, ws
+    # append and decode with append, on the decode workload's cache
+    dcfg = I.DECODE
+    qd_, kc_, vc_, pos_, qpos_ = I.decode_inputs(dcfg)
+    L = qpos_.astype(np.int64) + 1
+    qd, kcd, vcd = to_dev(qd_, device), to_dev(kc_, device), to_dev(vc_, device)
+    del kc_, vc_
+    posd = torch.from_numpy(pos_).to(device)
+    n_app = 512
+    kn = to_dev(I.normal_bf16(dcfg.seed * 16 + 11, (dcfg.B, n_app, dcfg.Hkv, dcfg.d)), device)
+    vn = to_dev(I.normal_bf16(dcfg.seed * 16 + 12, (dcfg.B, n_app, dcfg.Hkv, dcfg.d)), device)
+    p0a = torch.from_numpy(L.astype(np.int32)).to(device)
+
+    def append():
+        swa.swa_cache_append(kcd, vcd, posd, kn, vn, p0a, stream=stream)
+
+    ms = timed_steps(append, steps, warmup, flush, stream)
+    swa.swa_check_device_error()
+    nbytes = 2 * (2 * dcfg.B * n_app * dcfg.Hkv * dcfg.d * 2) + dcfg.B * n_app * 4 + dcfg.B * 4
+    out["cache_append"] = {"ms": ms, "bytes": nbytes, "launches_per_step": 1,
+                           "workload": f"{dcfg.name}: {n_app} tokens appended to each of {dcfg.B} sequences"}
+    del kn, vn
+    # decode with append: token at position L (the appended block moved the caches on;
+    # restore the decode workload's cache contents' positions first)
+    posd.copy_(torch.from_numpy(pos_).to(device))
+    qpos = torch.from_numpy(qpos_).to(device)
+    k1 = to_dev(I.normal_bf16(dcfg.seed * 16 + 13, (dcfg.B, dcfg.Hkv, dcfg.d)), device)
+    v1 = to_dev(I.normal_bf16(dcfg.seed * 16 + 14, (dcfg.B, dcfg.Hkv, dcfg.d)), device)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((dcfg.B, dcfg.Hq), dtype=torch.float32, device=device)
+    pdp = swa.decode_params(qd, kcd, vcd, posd, qpos, dcfg.scale, od, lsed, None)
+    wsd = torch.empty(swa.swa_decode_workspace_size(pdp), dtype=torch.uint8, device=device)
+
+    def dec_append():
+        swa.swa_decode_append(qd, kcd, vcd, posd, qpos, k1, v1, dcfg.scale, o=od, lse=lsed, workspace=wsd,
+                              stream=stream)
+
+    ms = timed_steps(dec_append, steps, warmup, flush, stream)
+    swa.swa_check_device_error()
+    out["decode_append"] = {"ms": ms, "bytes": decode_bytes(dcfg, L) + 2 * (2 * dcfg.B * dcfg.Hkv * dcfg.d * 2),
+                            "launches_per_step": 2,
+                            "workload": f"{dcfg.name}: the current token appended, then attended"}
+    return out
+
+
 def measure_e2e_prefill(cfg, steps, warmup, device, dev_tensors):
     """Same metric through the public call with host buffers: pinned H2D of q/k/v,
     swa_fwd, D2H of o and lse, every step, all inside the timed region."""
@@ -468,7 +553,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="comma list of workloads: mistral,decode,gemma,longformer,variants")
+                    help="comma list of workloads: mistral,decode,gemma,longformer,variants,cache")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -483,7 +568,8 @@ def main():
     torch.cuda.set_device(device)
     swa.load_library()
     hbm_peak, bf16_peak, peak_kind = load_peaks()
-    only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer", "variants"}
+    only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer", "variants",
+                                                         "cache"}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def barrier():
@@ -563,6 +649,21 @@ def main():
             "workload": I.DECODE.name, "variant": {"n_sink": 4}, "value": world * d["bytes"] / (dms * 1e-3) / 1e9,
             "unit": "GB/s", "ms_per_step": dms, "frac_of_hbm_peak": d["bytes"] / (dms * 1e-3) / 1e9 / hbm_peak}
         gpu_launches += d["launches_per_step"] * vsteps
+
+    if "cache" in only:
+        csteps = max(20, args.steps // 8)
+        cp = measure_cache_paths(csteps, args.warmup, device, flush)
+        for key, r in cp.items():
+            rms = max_over_ranks(float(r["ms"].mean()))
+            e = {"workload": r["workload"], "ms_per_step": rms}
+            if "flops" in r:
+                e.update({"value": world * r["flops"] / (rms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "frac_of_bf16_peak": r["flops"] / (rms * 1e-3) / 1e12 / bf16_peak})
+            else:
+                e.update({"value": world * r["bytes"] / (rms * 1e-3) / 1e9, "unit": "GB/s",
+                          "frac_of_hbm_peak": r["bytes"] / (rms * 1e-3) / 1e9 / hbm_peak})
+            secondary[key] = e
+            gpu_launches += r["launches_per_step"] * csteps
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

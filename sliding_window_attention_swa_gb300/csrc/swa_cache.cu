@@ -6,8 +6,7 @@
 // n_sink pinned sink slots in front: slot(p) = p for p < n_sink, else
 // n_sink + (p - n_sink) mod (n_slots - n_sink).
 //
-// Both kernels are pure copies, bound by HBM: one warp moves one (sequence, token,
-// kv head) pair of key and value rows in 16-byte pieces, grid-striding over pairs.
+// Both kernels are pure copies, bound by HBM, moving 16-byte pieces.
 #include <climits>
 
 #include "swa_internal.h"
@@ -20,87 +19,114 @@ constexpr unsigned int kErrBadPosition = 1u;    // a negative (or overflowing) p
 constexpr unsigned int kErrCacheMismatch = 2u;  // a slot not holding the position needed
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // independent 16-byte loads in flight per thread
 
-__device__ __forceinline__ void copy_rows(uint4 *kd, uint4 *vd, const uint4 *ks, const uint4 *vs, int pieces,
-                                          int lane) {
-    for (int c = lane; c < 2 * pieces; c += 32) {
-        if (c < pieces) kd[c] = ks ? __ldg(ks + c) : make_uint4(0, 0, 0, 0);
-        else vd[c - pieces] = vs ? __ldg(vs + c - pieces) : make_uint4(0, 0, 0, 0);
-    }
-}
+// Both kernels walk a flat list of 16-byte pieces: piece c of (sequence, token, kv
+// head) x is the c-th of the 2*D/8 pieces of its key row then its value row, so a
+// warp's lanes cover consecutive pieces of the same rows (coalesced).  Each thread
+// issues kUnroll loads before its stores.
 
+template <int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t total = static_cast<int64_t>(a.B) * a.n * a.H_kv;
-    const int pieces = a.D / 8;
+    constexpr int P = 2 * D / 8;
+    const int64_t total = static_cast<int64_t>(a.B) * a.n * a.H_kv * P;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t R = a.n_slots - a.n_sink;
-    for (int64_t x = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; x < total; x += nw) {
-        const int kvh = static_cast<int>(x % a.H_kv);
-        const int64_t bi = x / a.H_kv;
-        const int i = static_cast<int>(bi % a.n);
-        const int b = static_cast<int>(bi / a.n);
-        const int64_t p0 = __ldg(a.p0 + b);
-        const int64_t p = p0 + i, last = p0 + a.n - 1;
-        if (p0 < 0 || last > INT_MAX) {
-            if (lane == 0 && i == 0 && kvh == 0) atomicOr(&g_cache_err, kErrBadPosition);
-            continue;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+         base += kUnroll * stride) {
+        uint4 val[kUnroll];
+        uint4 *dst[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            dst[u] = nullptr;
+            const int64_t f = base + u * stride;
+            if (f >= total) continue;
+            const int c = static_cast<int>(f % P);
+            const int64_t x = f / P;
+            const int kvh = static_cast<int>(x % a.H_kv);
+            const int64_t bi = x / a.H_kv;
+            const int i = static_cast<int>(bi % a.n);
+            const int b = static_cast<int>(bi / a.n);
+            const int64_t p0 = __ldg(a.p0 + b);
+            const int64_t p = p0 + i, last = p0 + a.n - 1;
+            if (p0 < 0 || last > INT_MAX) {
+                if (c == 0 && i == 0 && kvh == 0) atomicOr(&g_cache_err, kErrBadPosition);
+                continue;
+            }
+            int64_t slot;
+            if (p < a.n_sink) {
+                slot = p;
+            } else {
+                if (last - p >= R) continue;  // a later token of this call takes the same ring slot
+                slot = a.n_sink + (p - a.n_sink) % R;
+            }
+            const bool is_v = c >= P / 2;
+            const int pc = is_v ? c - P / 2 : c;
+            const int64_t src = ((static_cast<int64_t>(b) * a.n + i) * a.H_kv + kvh) * D;
+            const int64_t dsto = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
+            val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
+            dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vc : a.kc) + dsto) + pc;
+            if (c == 0 && kvh == 0) a.slot_pos[static_cast<int64_t>(b) * a.n_slots + slot] = static_cast<int32_t>(p);
         }
-        int64_t slot;
-        if (p < a.n_sink) {
-            slot = p;
-        } else {
-            if (last - p >= R) continue;  // a later token of this call takes the same ring slot
-            slot = a.n_sink + (p - a.n_sink) % R;
-        }
-        const int64_t src = ((static_cast<int64_t>(b) * a.n + i) * a.H_kv + kvh) * a.D;
-        const int64_t dst = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * a.D;
-        copy_rows(reinterpret_cast<uint4 *>(a.kc + dst), reinterpret_cast<uint4 *>(a.vc + dst),
-                  reinterpret_cast<const uint4 *>(a.kn + src), reinterpret_cast<const uint4 *>(a.vn + src), pieces,
-                  lane);
-        if (kvh == 0 && lane == 0) a.slot_pos[static_cast<int64_t>(b) * a.n_slots + slot] = static_cast<int32_t>(p);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (dst[u]) *dst[u] = val[u];
     }
 }
 
 // Key index x of sequence b (0 <= x < Tk = W-1+C): x < W-1 is history position
 // p0 - (W-1) + x, read from its ring slot when the cache holds it; x >= W-1 is chunk
 // token x - (W-1).  Absent history rows are written as zeros and lie below kmin[b].
+template <int D>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    constexpr int P = 2 * D / 8;
     const int Tk = a.W - 1 + a.C;
-    const int64_t total = static_cast<int64_t>(a.B) * Tk * a.H_kv;
-    const int pieces = a.D / 8;
-    for (int64_t x = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; x < total; x += nw) {
-        const int kvh = static_cast<int>(x % a.H_kv);
-        const int64_t bx = x / a.H_kv;
-        const int xx = static_cast<int>(bx % Tk);
-        const int b = static_cast<int>(bx / Tk);
-        const int64_t p0 = __ldg(a.p0 + b);
-        const int64_t have = p0 < 0 ? 0 : min(min(p0, static_cast<int64_t>(a.n_slots)), static_cast<int64_t>(a.W - 1));
-        if (xx == 0 && kvh == 0 && lane == 0) {
-            a.kmin[b] = static_cast<int32_t>(a.W - 1 - have);
-            if (p0 < 0) atomicOr(&g_cache_err, kErrBadPosition);
-        }
-        const uint16_t *ks = nullptr, *vs = nullptr;
-        if (xx >= a.W - 1) {
-            const int64_t src = ((static_cast<int64_t>(b) * a.C + (xx - (a.W - 1))) * a.H_kv + kvh) * a.D;
-            ks = a.kn + src;
-            vs = a.vn + src;
-        } else if (xx >= a.W - 1 - have) {
-            const int64_t p = p0 - (a.W - 1) + xx;
-            const int64_t slot = p % a.n_slots;
-            if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
-                const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * a.D;
-                ks = a.kc + src;
-                vs = a.vc + src;
-            } else if (kvh == 0 && lane == 0) {
-                atomicOr(&g_cache_err, kErrCacheMismatch);
+    const int64_t total = static_cast<int64_t>(a.B) * Tk * a.H_kv * P;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+         base += kUnroll * stride) {
+        uint4 val[kUnroll];
+        uint4 *dst[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            dst[u] = nullptr;
+            const int64_t f = base + u * stride;
+            if (f >= total) continue;
+            const int c = static_cast<int>(f % P);
+            const int64_t x = f / P;
+            const int kvh = static_cast<int>(x % a.H_kv);
+            const int64_t bx = x / a.H_kv;
+            const int xx = static_cast<int>(bx % Tk);
+            const int b = static_cast<int>(bx / Tk);
+            const int64_t p0 = __ldg(a.p0 + b);
+            const int64_t have =
+                p0 < 0 ? 0 : min(min(p0, static_cast<int64_t>(a.n_slots)), static_cast<int64_t>(a.W - 1));
+            if (xx == 0 && kvh == 0 && c == 0) {
+                a.kmin[b] = static_cast<int32_t>(a.W - 1 - have);
+                if (p0 < 0) atomicOr(&g_cache_err, kErrBadPosition);
             }
+            const bool is_v = c >= P / 2;
+            const int pc = is_v ? c - P / 2 : c;
+            val[u] = make_uint4(0, 0, 0, 0);
+            if (xx >= a.W - 1) {
+                const int64_t src = ((static_cast<int64_t>(b) * a.C + (xx - (a.W - 1))) * a.H_kv + kvh) * D;
+                val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
+            } else if (xx >= a.W - 1 - have) {
+                const int64_t p = p0 - (a.W - 1) + xx;
+                const int64_t slot = p % a.n_slots;
+                if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
+                    const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
+                    val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
+                } else if (kvh == 0 && c == 0) {
+                    atomicOr(&g_cache_err, kErrCacheMismatch);
+                }
+            }
+            const int64_t dsto = ((static_cast<int64_t>(b) * Tk + xx) * a.H_kv + kvh) * D;
+            dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vl : a.kl) + dsto) + pc;
         }
-        const int64_t dst = ((static_cast<int64_t>(b) * Tk + xx) * a.H_kv + kvh) * a.D;
-        copy_rows(reinterpret_cast<uint4 *>(a.kl + dst), reinterpret_cast<uint4 *>(a.vl + dst),
-                  reinterpret_cast<const uint4 *>(ks), reinterpret_cast<const uint4 *>(vs), pieces, lane);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (dst[u]) *dst[u] = val[u];
     }
 }
 
@@ -115,24 +141,34 @@ int sm_count() {
     return n;
 }
 
-int copy_grid(int64_t warps) {
-    const int64_t blocks = (warps + kThreads / 32 - 1) / (kThreads / 32);
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 blocks of 8 warps per SM
+int copy_grid(int64_t pieces) {
+    const int64_t blocks = (pieces + kThreads * kUnroll - 1) / (kThreads * kUnroll);
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 blocks of 256 threads per SM
     return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
-    const int64_t warps = static_cast<int64_t>(a.B) * a.n * a.H_kv;
-    if (warps == 0) return cudaSuccess;
-    append_kernel<<<copy_grid(warps), kThreads, 0, s>>>(a);
+    const int64_t pieces = static_cast<int64_t>(a.B) * a.n * a.H_kv * (2 * a.D / 8);
+    if (pieces == 0) return cudaSuccess;
+    switch (a.D) {
+        case 64: append_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 128: append_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 256: append_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s) {
-    const int64_t warps = static_cast<int64_t>(a.B) * (a.W - 1 + a.C) * a.H_kv;
-    gather_kernel<<<copy_grid(warps), kThreads, 0, s>>>(a);
+    const int64_t pieces = static_cast<int64_t>(a.B) * (a.W - 1 + a.C) * a.H_kv * (2 * a.D / 8);
+    switch (a.D) {
+        case 64: gather_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 128: gather_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 256: gather_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
