@@ -107,28 +107,15 @@ struct BandKernelArgs {
     int64_t lse_st[3];
 };
 
-// Bit c of bits[] is set when key k0 + c (0 <= c < BN) is a global position; the
-// list is sorted, so a binary search finds its first entry >= k0.  Returns whether
-// any bit is set.
-template <int BN>
-__device__ __forceinline__ bool global_bits(const int32_t *g, int n, int k0, uint32_t (&bits)[BN / 32]) {
-#pragma unroll
-    for (int i = 0; i < BN / 32; ++i) bits[i] = 0u;
+// Index of the first entry >= k0 of the sorted list g[0..n) (n if none).
+__device__ __forceinline__ int first_at_least(const int32_t *g, int n, int k0) {
     int lo = 0, hi = n;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         if (__ldg(g + mid) < k0) lo = mid + 1;
         else hi = mid;
     }
-    bool any = false;
-    for (int i = lo; i < n; ++i) {
-        const int c = __ldg(g + i) - k0;
-        if (c >= BN) break;
-#pragma unroll
-        for (int wd = 0; wd < BN / 32; ++wd) bits[wd] |= (c >> 5) == wd ? (1u << (c & 31)) : 0u;
-        any = true;
-    }
-    return any;
+    return lo;
 }
 
 // Geometry of work unit u (units are numbered longest first).
@@ -496,14 +483,25 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     }
                     if (a.sep) {
                         // with separate global projections a global key is scored (with
-                        // k_g) in the global-column tiles only: drop it here
-                        uint32_t gb[BN / 32];
-                        if (global_bits<BN>(a.global_idx, a.n_global, k0, gb)) {
+                        // k_g) in the global-column tiles only: drop it here, 32 columns at
+                        // a time (the sorted list is scanned once from its first entry >= k0)
+                        int gi = first_at_least(a.global_idx, a.n_global, k0);
 #pragma unroll
-                            for (int c = 0; c < BN; ++c) {
-                                const bool g = (gb[c >> 5] >> (c & 31)) & 1u;
-                                count -= (g && x[c] != -INFINITY) ? 1 : 0;
-                                x[c] = g ? -INFINITY : x[c];
+                        for (int wd = 0; wd < BN / 32; ++wd) {
+                            uint32_t bits = 0u;
+                            while (gi < a.n_global) {
+                                const int c = __ldg(a.global_idx + gi) - k0 - 32 * wd;
+                                if (c >= 32) break;
+                                bits |= 1u << c;
+                                ++gi;
+                            }
+                            if (bits) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) {
+                                    const bool g = (bits >> e) & 1u;
+                                    count -= (g && x[32 * wd + e] != -INFINITY) ? 1 : 0;
+                                    x[32 * wd + e] = g ? -INFINITY : x[32 * wd + e];
+                                }
                             }
                         }
                     }
