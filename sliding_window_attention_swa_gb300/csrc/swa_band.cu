@@ -77,7 +77,10 @@ struct BandCfg {
     // o_done[2], o_free[2], pv_done[2], drain
     static constexpr int NBAR = 2 * NSLOT + 15;
     static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_TMEMPTR + 16 + 1024;  // + slack for 1024-B alignment
+    // global positions of a list of at most BN entries, staged once per CTA
+    static constexpr int OFF_GPOS = (OFF_TMEMPTR + 16 + 15) & ~15;
+    static constexpr int SMEM = OFF_GPOS + BN * 4 + 1024;  // + slack for 1024-B alignment
+    static_assert(OFF_GPOS + BN * 4 - OFF_BAR <= 2048, "barriers and staged positions exceed the reserve");
     static constexpr uint32_t TMEM_COLS = 512;
     __host__ __device__ static constexpr uint32_t tm_s(int slot) { return static_cast<uint32_t>(slot * BN); }
     __host__ __device__ static constexpr uint32_t tm_o(int tile) { return 256u + static_cast<uint32_t>(tile * 128); }
@@ -174,6 +177,11 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     auto bar_pv = [&](int i) { return bars + 8u * (12 + 2 * NSLOT + i); };
     const uint32_t bar_drain = bars + 8u * (14 + 2 * NSLOT);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
+    int *gpos = reinterpret_cast<int *>(sgen + C::OFF_GPOS);
+    // A list of at most BN positions is staged in shared memory for the global-column mask.
+    const bool gpos_staged = a.n_global > 0 && a.n_global <= BN;
+    if (gpos_staged)
+        for (int i = tid; i < a.n_global; i += C::THREADS) gpos[i] = a.global_idx[i];
 
     // ---- setup: barriers, TMEM (once per CTA)
     if (tid == 0) {
@@ -505,9 +513,35 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             }
                         }
                     }
+                } else if (gpos_staged) {
+                    // global columns, one tile of n <= BN sorted positions: those left of the
+                    // row's band form a prefix [0, nl) and those right of it a suffix [nr, n)
+                    // (two branch-free binary searches over the staged list); sinks keep only
+                    // the prefix, separate projections keep every column
+                    const int n = a.n_global;
+                    int nl = 0, nr = 0;
+#pragma unroll
+                    for (int step = BN; step >= 1; step >>= 1) {
+                        if (nl + step <= n && gpos[nl + step - 1] < lo_abs) nl += step;
+                        if (nr + step <= n && gpos[nr + step - 1] <= hi_abs) nr += step;
+                    }
+                    if (a.sink) nr = n;
+                    if (a.sep) nl = nr = n;
+                    count += nl + (n - nr);
+                    if (n <= 32) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            x[c] = (c < nl) | ((c >= nr) & (c < n)) ? x[c] : -INFINITY;
+#pragma unroll
+                        for (int c = 32; c < BN; ++c) x[c] = -INFINITY;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c)
+                            x[c] = (c < nl) | ((c >= nr) & (c < n)) ? x[c] : -INFINITY;
+                    }
                 } else {
-                    // global columns: each lane loads BN/32 of this tile's positions, shuffles
-                    // broadcast them; keep the ones outside the row's band
+                    // global columns of a longer list: each lane loads BN/32 of this tile's
+                    // positions, shuffles broadcast them; keep the ones outside the row's band
                     const int g0 = (j - w.n_band) * BN;
                     int gv[BN / 32];
 #pragma unroll
