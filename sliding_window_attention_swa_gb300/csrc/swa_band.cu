@@ -150,7 +150,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+template <int D, bool kGlob>  // kGlob: the launch has global positions (global-column tiles)
 __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     band_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const BandKernelArgs a) {
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
     int *gpos = reinterpret_cast<int *>(sgen + C::OFF_GPOS);
     // A list of at most BN positions is staged in shared memory for the global-column mask.
-    const bool gpos_staged = a.n_global > 0 && a.n_global <= BN;
+    const bool gpos_staged = kGlob && a.n_global > 0 && a.n_global <= BN;
     if (gpos_staged)
         for (int i = tid; i < a.n_global; i += C::THREADS) gpos[i] = a.global_idx[i];
 
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const int j = i >> 1;
                 const bool is_v = (i & 1) != 0;
                 const uint32_t dst = sRing + s * C::TBYTES;
-                if (j < w.n_band) {
+                if (!kGlob || j < w.n_band) {
                     if (lane == 0) {
                         const int k0 = w.kv_lo + j * BN;
                         mbar_arrive_expect_tx(bar_full(s), C::TBYTES);
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(raw[c][e]);
                 }
                 // ---- mask (branch-free; only band-edge and global tiles)
-                if (j < w.n_band) {
+                if (!kGlob || j < w.n_band) {
                     const int k0 = w.kv_lo + j * BN;
                     const bool interior = (a.wl < 0 || k0 >= thi - a.wl) && (a.wr < 0 || k0 + BN - 1 <= tlo + a.wr) &&
                                           (k0 + BN - 1 <= a.Tk - 1);
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         for (int c = 0; c < BN; ++c)
                             x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
                     }
-                    if (a.sep) {
+                    if (kGlob && a.sep) {
                         // with separate global projections a global key is scored (with
                         // k_g) in the global-column tiles only: drop it here, 32 columns at
                         // a time (the sorted list is scanned once from its first entry >= k0)
@@ -734,11 +734,14 @@ int band_sm_count() {
 template <int D>
 cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     using C = BandCfg<D>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(band_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    // launches without global positions take the kernel built without their code paths
+    const bool glob = x.n_global > 0;
+    auto kernel = glob ? band_fwd_kernel<D, true> : band_fwd_kernel<D, false>;
+    static bool configured[2] = {false, false};
+    if (!configured[glob]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[glob] = true;
     }
     const int G = x.H_q / x.H_kv;
     const int TQ = BM / G;
@@ -782,7 +785,7 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
     a.n_units = static_cast<int>(units);
     const int grid = static_cast<int>(units < band_sm_count() ? units : band_sm_count());
-    band_fwd_kernel<D><<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
+    kernel<<<grid, C::THREADS, C::SMEM, s>>>(mq, mk, mv, a);
     return cudaGetLastError();
 }
 
