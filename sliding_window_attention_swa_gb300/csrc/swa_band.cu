@@ -60,12 +60,13 @@ struct BandCfg {
     // NQT = 2: warpgroup 0 = K/V producer warp, MMA warp, Q loader warp, one idle
     // warp; warpgroups 1, 2 = softmax.  Twelve warps put three on each SM
     // sub-partition, whose 16K-register file caps the launch at 168 registers a
-    // thread; setmaxnreg then moves registers from warpgroup 0 (88) to the softmax
-    // warpgroups (208):  128 * 88 + 256 * 208 = 64512 = 384 * 168.
+    // thread; setmaxnreg then moves registers from warpgroup 0 (104) to the softmax
+    // warpgroups (200):  128 * 104 + 256 * 200 = 64512 = 384 * 168.  (Neither side
+    // spills; control warps below 104 spill in the producer's gather.)
     // NQT = 1: the same warpgroup 0, then one softmax warpgroup (256 threads).
     static constexpr int THREADS = NQT == 2 ? 384 : 256;
     static constexpr int SOFTMAX_WARP0 = 4;
-    static constexpr int REG_CTRL = 88, REG_SOFTMAX = 208;
+    static constexpr int REG_CTRL = 104, REG_SOFTMAX = 200;
     static_assert(NQT == 1 || 128 * REG_CTRL + 256 * REG_SOFTMAX <= THREADS * 168, "register split");
     static constexpr int QBYTES = BM * D * 2;  // one query tile
     static constexpr int TBYTES = BN * D * 2;  // one K or V tile
