@@ -106,6 +106,7 @@ struct BandKernelArgs {
     const __nv_bfloat16 *k, *v;  // for the global-column gather (k_g, v_g when sep)
     int64_t k_st[3], v_st[3], o_st[3];
     __nv_bfloat16 *o;
+    int o_align32;  // o and its strides are 32-byte aligned: rows stored 32 bytes at a time
     float *lse;
     int32_t *counts;
     int64_t lse_st[3];
@@ -652,7 +653,18 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 uint32_t ov[32];
                 tmem_ld32(o_addr + c * 32, ov);
                 tc_wait_ld();
-                if (row_ok) {
+                if (row_ok && a.o_align32) {
+                    // 32-byte stores: each lane of a store writes one whole sector of its row
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8) {
+                        uint32_t wv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            wv[e] = pack_bf16x2(__uint_as_float(ov[q8 * 16 + 2 * e]) * inv_l,
+                                                __uint_as_float(ov[q8 * 16 + 2 * e + 1]) * inv_l);
+                        st_global_v8(orow + c * 32 + q8 * 16, wv);
+                    }
+                } else if (row_ok) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint32_t wv[4];
@@ -780,6 +792,8 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
         a.lse_st[i] = x.lse_st[i];
     }
     a.o = static_cast<__nv_bfloat16 *>(x.o);
+    a.o_align32 = (reinterpret_cast<uintptr_t>(x.o) % 32 == 0) && (x.o_st[0] % 16 == 0) && (x.o_st[1] % 16 == 0) &&
+                  (x.o_st[2] % 16 == 0);
     a.lse = x.lse;
     a.counts = x.counts;
     const long long units = static_cast<long long>(x.B) * x.H_kv * a.n_units_t;

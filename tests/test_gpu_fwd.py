@@ -88,6 +88,27 @@ def test_strided_inputs():
     assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, "strided")
 
 
+def test_output_with_16_byte_alignment():
+    """O written through a view whose base and row strides are 16- but not 32-byte
+    aligned (the kernel then stores 16 bytes at a time)."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    B, T, Hq, Hkv, d = 1, 300, 4, 2, 128
+    q = I.normal_bf16(911, (B, T, Hq, d))
+    k = I.normal_bf16(912, (B, T, Hkv, d))
+    v = I.normal_bf16(913, (B, T, Hkv, d))
+    buf = torch.zeros((B, T, Hq, d + 8), dtype=torch.bfloat16, device="cuda")
+    o = buf[..., 8:]  # 16 bytes past a 256-byte aligned base; row stride 272 bytes
+    _, lse, cnt = swa.swa_fwd(to_dev(q), to_dev(k), to_dev(v), 40, 0, d ** -0.5, o=o, want_counts=True)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, 40, 0, d ** -0.5)
+    assert_parity(to_host_f64(o).transpose(0, 2, 1, 3), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref,
+                  cnt_ref, "16-byte aligned O")
+    assert (buf[..., :8] == 0).all()  # nothing written outside the view
+
+
 def _closed_form_counts(T, wl, wr, G):
     t = np.arange(T)
     lo = np.zeros(T, dtype=np.int64) if wl < 0 else np.maximum(0, t - wl)
