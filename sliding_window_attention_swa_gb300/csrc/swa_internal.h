@@ -59,7 +59,7 @@ struct MergeArgs {
 
 // Split geometry shared by the workspace-size query and the launch.
 constexpr int kSplitChunk = 64;         // slots per pipeline stage
-constexpr int kSlotsPerSplit = 512;     // slots per CTA
+constexpr int kSlotsPerSplit = 1024;    // slots per work item (larger items amortise the per-item combine)
 constexpr int kSplitRows = 16;          // mma.sync M: query rows per CTA
 
 inline int split_q_per_cta(int group) { return group >= kSplitRows ? 1 : kSplitRows / group; }

@@ -10,7 +10,7 @@
 //
 // Persistent kernel, two CTAs per SM for head dim <= 128 (one for 256), five warps:
 //   warp 0     producer.  Walks this CTA's work items (batch, kv head, query block,
-//              512-slot split) in a static round-robin order.  For each item it
+//              1024-slot split) in a static round-robin order.  For each item it
 //              reads the slot positions, builds one 64-bit validity mask per
 //              64-slot chunk, writes the split's valid count, and streams the K and
 //              V of every chunk that has a valid slot into a ring of NST stages
@@ -40,7 +40,7 @@ namespace {
 __device__ unsigned int g_split_err = 0;
 
 constexpr int CH = kSplitChunk;                 // slots per chunk (64)
-constexpr int MAX_CHUNKS = kSlotsPerSplit / CH;  // chunks per split (8)
+constexpr int MAX_CHUNKS = kSlotsPerSplit / CH;  // chunks per split (16)
 constexpr int kThreads = 160;
 
 struct StageHdr {

@@ -71,9 +71,10 @@ def test_decode_noalloc_rejects_oversized_problem():
     import sliding_window_attention_swa_gb300 as swa
 
     lib = _noalloc_lib()
-    # 16 sequences x 128 query heads x 8 splits x 256 dims of fp32 partials: > 16 MiB.
-    # The buffers are full size, so the call would stay in bounds even if it ran.
-    B, Hq, Hkv, d, W = 16, 128, 8, 256, 4096
+    # 40 sequences x 128 query heads x 4 splits (1024 slots each) x 256 dims of fp32
+    # partials: > 16 MiB.  The buffers are full size, so the call would stay in bounds
+    # even if it ran.
+    B, Hq, Hkv, d, W = 40, 128, 8, 256, 4096
     q = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(B, Hkv, W, d, dtype=torch.bfloat16, device="cuda")
     pos = torch.zeros(B, W, dtype=torch.int32, device="cuda")
