@@ -367,40 +367,65 @@ def measure_cache_paths(steps, warmup, device, flush):
 
 
 def measure_e2e_prefill(cfg, steps, warmup, device, dev_tensors):
-    """Same metric through the public call with host buffers: pinned H2D of q/k/v,
-    swa_fwd, D2H of o and lse, every step, all inside the timed region."""
+    """Same metric through the public call with host buffers, as a serving loop runs it:
+    every step copies its q/k/v from pinned host memory to the device, calls swa_fwd and
+    copies o and lse back to pinned host memory, all inside the timed region.  Steps are
+    double-buffered on three streams, so step i+1's upload and step i-1's download
+    overlap step i's kernel (each buffer set is reused only after its previous step's
+    kernel and download are done)."""
     import torch
     import sliding_window_attention_swa_gb300 as swa
 
-    qd, kd, vd, g, o, lse, ws = dev_tensors
-    hq = torch.empty(qd.shape, dtype=qd.dtype, pin_memory=True).copy_(qd)
-    hk = torch.empty(kd.shape, dtype=kd.dtype, pin_memory=True).copy_(kd)
-    hv = torch.empty(vd.shape, dtype=vd.dtype, pin_memory=True).copy_(vd)
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    stream = torch.cuda.current_stream()
+    qd0, kd0, vd0, g, o0, lse0, ws0 = dev_tensors
+    hq = torch.empty(qd0.shape, dtype=qd0.dtype, pin_memory=True).copy_(qd0)
+    hk = torch.empty(kd0.shape, dtype=kd0.dtype, pin_memory=True).copy_(kd0)
+    hv = torch.empty(vd0.shape, dtype=vd0.dtype, pin_memory=True).copy_(vd0)
+    sets = [(qd0, kd0, vd0, o0, lse0, ws0)]
+    sets.append((torch.empty_like(qd0), torch.empty_like(kd0), torch.empty_like(vd0), torch.empty_like(o0),
+                 torch.empty_like(lse0), torch.empty_like(ws0)))
+    host_out = [(torch.empty(o0.shape, dtype=o0.dtype, pin_memory=True),
+                 torch.empty(lse0.shape, dtype=lse0.dtype, pin_memory=True)) for _ in range(2)]
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ran = [torch.cuda.Event() for _ in range(2)]    # kernel of the set's last step done
+    loaded = [torch.cuda.Event() for _ in range(2)]  # inputs of the set's current step on the device
+    saved = [torch.cuda.Event() for _ in range(2)]   # outputs of the set's last step on the host
 
-    def run():
-        qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
+    def step(i):
+        x = i % 2
+        qd, kd, vd, o, lse, ws = sets[x]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ran[x])
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            loaded[x].record(s_in)
+        s_run.wait_event(loaded[x])
+        if i >= 2:
+            s_run.wait_event(saved[x])
         swa.swa_fwd(qd, kd, vd, cfg.window_left, cfg.window_right, cfg.scale, g, o=o, lse=lse, workspace=ws,
-                    stream=stream)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+                    stream=s_run)
+        ran[x].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ran[x])
+            host_out[x][0].copy_(o, non_blocking=True)
+            host_out[x][1].copy_(lse, non_blocking=True)
+            saved[x].record(s_out)
 
-    for _ in range(warmup):
-        run()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        run()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(steps):
+        step(i)
+    s_out.wait_event(ran[(steps - 1) % 2])
+    b.record(s_out)  # after the last step's download (the last work of the pipeline)
     torch.cuda.synchronize()
+    swa.swa_check_device_error()
     ms = a.elapsed_time(b) / steps
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     return ms, h2d, d2h
 
 
