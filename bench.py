@@ -32,6 +32,16 @@ sys.path.insert(0, ROOT)
 from sliding_window_attention_swa_gb300 import inputs as I  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+METRIC = "SWA prefill band-TFLOP/s (Mistral-shape causal prefill); decode GB/s in secondary"
+
+
+def headline_config(world: int) -> dict:
+    """The headline workload's config, identical in both arms."""
+    c = I.MISTRAL
+    return {"workload": c.name, "B": c.B, "T": c.T, "H_q": c.Hq, "H_kv": c.Hkv, "d_h": c.d,
+            "window": c.window_left + 1, "causal": True,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed (256 MB write) before every timed step", "flops_per_step": prefill_flops(c)}
 KERNELS = {"band": "band_fwd_kernel", "split": "stream_attn_kernel", "merge": "merge_kernel"}
 
 
@@ -556,12 +566,11 @@ def run_reference(args):
             vals.append((v, n, dt, sampler.threads()))
     value = float(np.mean([x[0] for x in vals]))
     line = {
-        "impl": "reference", "metric": "SWA prefill band-TFLOP/s (fp64 CPU oracle, bounded row sample)",
+        "impl": "reference", "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": float(np.mean([x[2] for x in vals]) * 1e3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "H_q": cfg.Hq, "H_kv": cfg.Hkv, "d_h": cfg.d,
-                   "window": cfg.window_left + 1},
+        "config": headline_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0][3], "kind": "oracle",
                          "sample": f"about {int(np.mean([x[1] for x in vals]))} random query rows of the "
                                    f"workload per step ({budget:.2f} s of fp64 work)"},
@@ -701,15 +710,11 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": "SWA prefill band-TFLOP/s (Mistral-shape causal prefill); decode GB/s in secondary",
+            "metric": METRIC,
             "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": I.MISTRAL.name, "B": I.MISTRAL.B, "T": I.MISTRAL.T, "H_q": I.MISTRAL.Hq,
-                       "H_kv": I.MISTRAL.Hkv, "d_h": I.MISTRAL.d, "window": I.MISTRAL.window_left + 1,
-                       "causal": True, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed (256 MB write) before every timed step",
-                       "flops_per_step": flops},
+            "config": headline_config(world),
             "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": kernel_tflops / bf16_peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)", "kernel": KERNELS["band"]},
