@@ -100,6 +100,7 @@ CHUNK = [
     (2, 129, 8, 8, 64, 128, 200, [5, 700]),        # ring longer than the window
     (2, 64, 4, 1, 256, 128, 40, [10, 300]),        # ring shorter than the window
     (1, 600, 4, 2, 128, 100, 100, [3000]),         # chunk longer than the window
+    (2, 1, 8, 2, 128, 64, 64, [0, 500]),           # one-token chunks, one without history
 ]
 
 

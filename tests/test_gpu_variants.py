@@ -198,3 +198,36 @@ def test_decode_sinks_and_window(W, ns, d):
     assert_parity(to_host_f64(o), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref, cnt_ref, f"W{W} ns{ns}")
     want = np.minimum(L, W) + np.maximum(0, np.minimum(ns, L - W))
     assert (cnt.cpu().numpy() == want[:, None]).all()
+
+
+def test_decode_rows_without_valid_slots():
+    """A sequence whose every slot is stale or in the future: the empty row gives
+    O = 0, lse = -inf and count 0 (the empty-set reading of the mask); other
+    sequences of the same call are unaffected."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    B, Hq, Hkv, d, W = 3, 8, 2, 128, 256
+    q = I.normal_bf16(71, (B, Hq, d))
+    kc = I.normal_bf16(72, (B, Hkv, W, d))
+    vc = I.normal_bf16(73, (B, Hkv, W, d))
+    pos = I.ring_slot_positions(np.array([300, 5, 1000]), W)
+    pos[1, :] = -1          # never written
+    pos[2, :] = 5000        # every slot after the query position
+    qpos = np.array([299, 4, 999], dtype=np.int32)
+    o, lse, cnt = swa.swa_decode(to_dev(q), to_dev(kc), to_dev(vc), i32_dev(pos), i32_dev(qpos), d ** -0.5,
+                                 want_counts=True)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o_ref, lse_ref, cnt_ref = oracle.decode(q, kc, vc, pos, qpos, d ** -0.5)
+    assert (cnt_ref[1:] == 0).all()
+    assert_parity(to_host_f64(o), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref, cnt_ref, "empty rows")
+    assert (to_host_f64(o)[1:] == 0).all()
+
+
+def test_gqa_group_16_head_dim_256():
+    B, T, Hq, Hkv, d = 1, 200, 16, 1, 256
+    q, k, v = _inputs(81, B, T, Hq, Hkv, d)
+    o, lse, cnt = _run(q, k, v, 50, 0, d ** -0.5)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, 50, 0, d ** -0.5)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, "G=16 d=256")
