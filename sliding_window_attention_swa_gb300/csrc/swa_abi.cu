@@ -248,7 +248,7 @@ cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s
     sa.W = p->window > 0 ? p->window : p->W;
     sa.n_sink = p->n_sink;
     sa.scale_log2 = p->scale * kLog2e;
-    sa.slots_per_split = kSlotsPerSplit;
+    sa.slots_per_split = split_size(p->W);
     sa.n_splits = split_count(p->W);
     sa.q_per_cta = split_q_per_cta(p->H_q / p->H_kv);
     split_carve(ws, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
@@ -385,7 +385,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         sa.W = p->T;
         sa.n_sink = 0;
         sa.scale_log2 = scale_log2;
-        sa.slots_per_split = swa::kSlotsPerSplit;
+        sa.slots_per_split = swa::split_size(p->T);
         sa.n_splits = swa::split_count(p->T);
         sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
         swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T, &sa.ws_ml, &sa.ws_acc,

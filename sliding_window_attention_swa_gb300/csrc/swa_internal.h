@@ -64,6 +64,13 @@ constexpr int kSplitRows = 16;          // mma.sync M: query rows per CTA
 
 inline int split_q_per_cta(int group) { return group >= kSplitRows ? 1 : kSplitRows / group; }
 inline int split_count(int n_slots) { return (n_slots + kSlotsPerSplit - 1) / kSlotsPerSplit; }
+// Slots per split: the fewest whole chunks that still cover n_slots with split_count
+// splits, so the last split is not left nearly empty (4100 slots: 5 x 832, not 4 x 1024 + 4).
+inline int split_size(int n_slots) {
+    const int ns = split_count(n_slots);
+    const int per = (n_slots + ns - 1) / ns;
+    return (per + kSplitChunk - 1) / kSplitChunk * kSplitChunk;
+}
 inline size_t split_workspace_bytes(int B, int NQ, int H_q, int H_kv, int D, int n_slots) {
     const size_t ns = static_cast<size_t>(split_count(n_slots));
     const size_t rows = static_cast<size_t>(B) * NQ * H_q * ns;

@@ -549,7 +549,9 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    if (a.slots_per_split != kSlotsPerSplit) return cudaErrorInvalidValue;
+    if (a.slots_per_split <= 0 || a.slots_per_split > kSlotsPerSplit || a.slots_per_split % CH != 0 ||
+        static_cast<int64_t>(a.slots_per_split) * a.n_splits < a.n_slots)
+        return cudaErrorInvalidValue;
     CUtensorMap mk, mv;
     if (!slot_map(&mk, a.k, D, a.n_slots, a.H_kv, a.B, a.k_ss, a.k_sh, a.k_sb) ||
         !slot_map(&mv, a.v, D, a.n_slots, a.H_kv, a.B, a.v_ss, a.v_sh, a.v_sb))
