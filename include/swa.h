@@ -235,19 +235,22 @@ SWA_API swa_status swa_decode_append(const swa_decode_params *p, const void *k_n
  * Chunked prefill against a ring cache: C new tokens per sequence, at positions
  * p0[b] .. p0[b] + C - 1, attend to the cached history and to the chunk itself; the
  * query at position t keeps the keys at positions t - window < p <= t (lizeman page,
- * section 2 window; the cache convention above).
+ * section 2 window; the cache convention above) and, for a cache with n_sink pinned
+ * sinks, the sink positions p < n_sink with p <= t (the rule of swa_decode).
  *   q            bf16 [B, C, H_q, d_h], contiguous
  *   k_new, v_new bf16 [B, C, H_kv, d_h], contiguous: the chunk's keys and values
  *   p0           device int32 [B]: position of each sequence's first chunk token
  *   o            bf16 [B, C, H_q, d_h]; lse fp32 [B, H_q, C]; row_counts optional [B, H_q, C]
  *   append       nonzero: afterwards append the chunk to the cache (swa_cache_append)
  * The cache must hold, for every sequence, every position in
- * [max(0, p0 - n_slots), p0) -- the tokens appended before the chunk; a slot found
- * holding another position is reported by swa_check_device_error as
- * SWA_ERR_INVALID_ARG.  Requirements: the cache's B, H_kv, d_h match; n_sink = 0
- * (a sink cache is SWA_ERR_UNSUPPORTED here); window >= 1; H_q / H_kv <= 16.
- * Workspace: swa_prefill_chunk_workspace_size bytes, 256-byte aligned (the chunk's
- * key/value rows and the window history gathered in position order).
+ * [max(0, p0 - n_slots), p0) (with sinks: the sinks and the last n_slots - n_sink
+ * positions) -- the tokens appended before the chunk; a slot found holding another
+ * position is reported by swa_check_device_error as SWA_ERR_INVALID_ARG.
+ * Requirements: the cache's B, H_kv, d_h match; window >= 1; H_q / H_kv <= 16; with
+ * sinks, n_sink <= 128 and a ring of at least window - 1 slots (n_slots - n_sink), else
+ * SWA_ERR_UNSUPPORTED.  Workspace: swa_prefill_chunk_workspace_size bytes, 256-byte
+ * aligned (the chunk's key/value rows and the window history gathered in position
+ * order, and the sinks' rows).
  */
 typedef struct swa_chunk_params {
     const void *q;

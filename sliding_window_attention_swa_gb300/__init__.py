@@ -405,10 +405,10 @@ def chunk_params(q, k_new, v_new, p0, window: int, scale: float, o, lse, row_cou
 
 def swa_prefill_chunk(q, k_new, v_new, k_cache, v_cache, slot_pos, p0, window: int, scale: float | None = None, *,
                       append: bool = False, o=None, lse=None, want_counts: bool = False, workspace=None,
-                      stream=None):
+                      stream=None, n_sink: int = 0):
     """Chunked prefill: q [B,C,H_q,d] and the chunk's k_new/v_new [B,C,H_kv,d] at positions
-    p0[b] + i attend to the ring cache's history and to the chunk (causal window).
-    append: afterwards the chunk joins the cache.  Returns (o [B,C,H_q,d], lse [B,H_q,C],
+    p0[b] + i attend to the ring cache's history and to the chunk (causal window), and to
+    the cache's n_sink pinned sinks.  append: afterwards the chunk joins the cache.  Returns (o [B,C,H_q,d], lse [B,H_q,C],
     row_counts or None)."""
     import torch
 
@@ -427,7 +427,7 @@ def swa_prefill_chunk(q, k_new, v_new, k_cache, v_cache, slot_pos, p0, window: i
     lse = torch.empty((B, Hq, C), dtype=torch.float32, device=q.device) if lse is None else lse
     row_counts = torch.empty((B, Hq, C), dtype=torch.int32, device=q.device) if want_counts else None
     p = chunk_params(q, k_new, v_new, p0, window, scale, o, lse, row_counts, append)
-    c = cache_params(k_cache, v_cache, slot_pos)
+    c = cache_params(k_cache, v_cache, slot_pos, n_sink)
     need = int(lib.swa_prefill_chunk_workspace_size(ctypes.byref(p), ctypes.byref(c)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

@@ -99,7 +99,9 @@ swa_status chunk_check(const swa_chunk_params *p, const swa_cache_params *c) {
     if (p->H_q % p->H_kv != 0 || p->B != c->B || p->H_kv != c->H_kv || p->d_h != c->d_h) return SWA_ERR_INVALID_ARG;
     if (!std::isfinite(p->scale)) return SWA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(p->window) - 1 + p->C > (1 << 30)) return SWA_ERR_INVALID_ARG;
-    if (c->n_sink != 0) return SWA_ERR_UNSUPPORTED;
+    // a sink cache's ring must cover the window (its history is then contiguous)
+    if (c->n_sink > 0 && c->n_slots - c->n_sink < p->window - 1) return SWA_ERR_UNSUPPORTED;
+    if (c->n_sink > 128) return SWA_ERR_UNSUPPORTED;
     if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
     if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
     if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
@@ -110,15 +112,17 @@ swa_status chunk_check(const swa_chunk_params *p, const swa_cache_params *c) {
     return SWA_OK;
 }
 
-// Workspace of a chunked prefill: gathered keys, gathered values, kmin.
+// Workspace of a chunked prefill: gathered keys and values, kmin, sink rows, sink list.
 struct ChunkWs {
-    size_t kv_bytes, total;
+    size_t kv_bytes, kmin_bytes, sink_bytes, total;
 };
-ChunkWs chunk_ws(const swa_chunk_params *p) {
+ChunkWs chunk_ws(const swa_chunk_params *p, const swa_cache_params *c) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t rows = static_cast<size_t>(p->B) * (static_cast<size_t>(p->window) - 1 + p->C) * p->H_kv;
     const size_t kv = up(rows * p->d_h * 2);
-    return {kv, 2 * kv + up(static_cast<size_t>(p->B) * 4)};
+    const size_t km = up(static_cast<size_t>(p->B) * 4);
+    const size_t sk = up(static_cast<size_t>(p->B) * c->n_sink * p->H_kv * p->d_h * 2);
+    return {kv, km, sk, 2 * kv + km + 2 * sk + up(static_cast<size_t>(c->n_sink) * 4)};
 }
 
 swa::AppendArgs append_args(const swa_cache_params *c, const void *k_new, const void *v_new, int n,
@@ -461,14 +465,14 @@ swa_status swa_decode_append(const swa_decode_params *p, const void *k_new, cons
 
 size_t swa_prefill_chunk_workspace_size(const swa_chunk_params *p, const swa_cache_params *c) {
     if (chunk_check(p, c) != SWA_OK) return 0;
-    return chunk_ws(p).total;
+    return chunk_ws(p, c).total;
 }
 
 swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *c, void *workspace,
                              size_t workspace_bytes, swa_stream_t stream) {
     swa_status st = chunk_check(p, c);
     if (st != SWA_OK) return st;
-    const ChunkWs ws = chunk_ws(p);
+    const ChunkWs ws = chunk_ws(p, c);
     st = workspace_ok(workspace, workspace_bytes, ws.total);
     if (st != SWA_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -477,6 +481,10 @@ swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *
     uint16_t *kl = reinterpret_cast<uint16_t *>(w);
     uint16_t *vl = reinterpret_cast<uint16_t *>(w + ws.kv_bytes);
     int32_t *kmin = reinterpret_cast<int32_t *>(w + 2 * ws.kv_bytes);
+    uint16_t *ksink = reinterpret_cast<uint16_t *>(w + 2 * ws.kv_bytes + ws.kmin_bytes);
+    uint16_t *vsink = reinterpret_cast<uint16_t *>(w + 2 * ws.kv_bytes + ws.kmin_bytes + ws.sink_bytes);
+    int32_t *sink_idx = reinterpret_cast<int32_t *>(w + 2 * ws.kv_bytes + ws.kmin_bytes + 2 * ws.sink_bytes);
+    const int ns = c->n_sink;
 
     // 1. the window history (positions p0-W+1 .. p0-1) in position order, then the chunk
     swa::GatherArgs ga{};
@@ -487,6 +495,10 @@ swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *
     ga.H_kv = p->H_kv;
     ga.D = p->d_h;
     ga.n_slots = c->n_slots;
+    ga.n_sink = ns;
+    ga.ks = ksink;
+    ga.vs = vsink;
+    ga.sink_idx = sink_idx;
     ga.kn = static_cast<const uint16_t *>(p->k_new);
     ga.vn = static_cast<const uint16_t *>(p->v_new);
     ga.C = C;
@@ -523,6 +535,19 @@ swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *
     ba.scale_log2 = p->scale * kLog2e;
     ba.kg = kl;
     ba.vg = vl;
+    if (ns > 0) {
+        // the sinks as pinned key columns: true positions 0 .. ns-1 against each row's band
+        // (key index W-1 is position p0[b]); their rows are the gathered sink rows
+        ba.global_idx = sink_idx;
+        ba.n_global = ns;
+        ba.gmode = SWA_GLOBAL_SINK;
+        ba.p0 = p->p0;
+        ba.gcol_list_rows = true;
+        ba.kg = ksink;
+        ba.vg = vsink;
+        const int64_t ss[3] = {static_cast<int64_t>(ns) * p->H_kv * D, p->H_kv * D, D};
+        for (int i = 0; i < 3; ++i) ba.kg_st[i] = ba.vg_st[i] = ss[i];
+    }
     ba.lse = p->lse;
     ba.counts = p->row_counts;
     ba.lse_st[0] = static_cast<int64_t>(p->H_q) * C;

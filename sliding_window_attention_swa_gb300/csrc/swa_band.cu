@@ -96,6 +96,10 @@ struct BandKernelArgs {
     // index t + q_off, and keys below kmin[b] (when kmin is set) do not exist.
     int Tk, q_off;
     const int32_t *kmin;
+    // key index q_off of sequence b is position p0[b] (nullptr: 0); global positions are
+    // positions, and with gcol_list_rows their K/V rows are the k/v rows in list order
+    const int32_t *p0;
+    int gcol_list_rows;
     int wl, wr;
     float scale_log2;
     const int32_t *global_idx;
@@ -126,6 +130,7 @@ __device__ __forceinline__ int first_at_least(const int32_t *g, int n, int k0) {
 // Geometry of work unit u (units are numbered longest first).
 struct Unit {
     int b, kvh, t0, kv_lo, n_band, n_tiles, kmin;
+    int pos_off;  // position of key index x is x + pos_off
 };
 
 template <int NQT, int BN>
@@ -138,6 +143,7 @@ __device__ __forceinline__ Unit unit_of(int u, const BandKernelArgs &a) {
     w.t0 = ut * NQT * a.TQ;
     const int t1 = min(a.T - 1, w.t0 + NQT * a.TQ - 1);
     w.kmin = a.kmin ? __ldg(a.kmin + w.b) : 0;
+    w.pos_off = a.p0 ? __ldg(a.p0 + w.b) - a.q_off : 0;
     w.kv_lo = a.wl < 0 ? w.kmin : max(w.kmin, w.t0 + a.q_off - a.wl);
     const int kv_hi = a.wr < 0 ? a.Tk - 1 : min(a.Tk - 1, t1 + a.q_off + a.wr);
     w.n_band = (kv_hi - w.kv_lo + BN) / BN;
@@ -255,8 +261,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         const int gi = g0 + r;
                         int srow = -1;
                         if (gi < a.n_global) {
-                            const int gs = a.global_idx[gi];
-                            if (gs >= 0 && gs < a.Tk) srow = gs;
+                            if (a.gcol_list_rows) {
+                                srow = gi;
+                            } else {
+                                const int gs = a.global_idx[gi];
+                                if (gs >= 0 && gs < a.Tk) srow = gs;
+                            }
                         }
                         uint4 val = make_uint4(0, 0, 0, 0);
                         if (srow >= 0)
@@ -521,11 +531,13 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     // (two branch-free binary searches over the staged list); sinks keep only
                     // the prefix, separate projections keep every column
                     const int n = a.n_global;
+                    // (positions: the band's key indices shifted by the sequence's offset)
+                    const int lo_pos = lo_abs + w.pos_off, hi_pos = hi_abs + w.pos_off;
                     int nl = 0, nr = 0;
 #pragma unroll
                     for (int step = BN; step >= 1; step >>= 1) {
-                        if (nl + step <= n && gpos[nl + step - 1] < lo_abs) nl += step;
-                        if (nr + step <= n && gpos[nr + step - 1] <= hi_abs) nr += step;
+                        if (nl + step <= n && gpos[nl + step - 1] < lo_pos) nl += step;
+                        if (nr + step <= n && gpos[nr + step - 1] <= hi_pos) nr += step;
                     }
                     if (a.sink) nr = n;
                     if (a.sep) nl = nr = n;
@@ -557,8 +569,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         const int gs = __shfl_sync(0xffffffffu, gv[c >> 5], c & 31);
                         // kept: outside the row's band (sinks: left of it); with separate
                         // projections every global key is scored here
-                        const bool outside = (gs < lo_abs) | ((gs > hi_abs) & !a.sink);
-                        const bool al = (gs >= 0) & (gs < a.Tk) & (outside | (a.sep != 0));
+                        const bool outside =
+                            (gs < lo_abs + w.pos_off) | ((gs > hi_abs + w.pos_off) & !a.sink);
+                        const bool valid = a.gcol_list_rows ? gs >= 0 : (gs >= 0) & (gs < a.Tk);
+                        const bool al = valid & (outside | (a.sep != 0));
                         cnt4[c & 3] += al ? 1 : 0;
                         x[c] = al ? x[c] : -INFINITY;
                     }
@@ -770,6 +784,8 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.Tk = Tk;
     a.q_off = x.q_off;
     a.kmin = x.kmin;
+    a.p0 = x.p0;
+    a.gcol_list_rows = x.gcol_list_rows ? 1 : 0;
     a.H_q = x.H_q;
     a.H_kv = x.H_kv;
     a.G = G;
@@ -783,11 +799,13 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.n_global = x.n_global;
     a.sink = x.gmode == SWA_GLOBAL_SINK ? 1 : 0;
     a.sep = x.sep ? 1 : 0;
-    a.k = static_cast<const __nv_bfloat16 *>(x.sep ? x.kg : x.k);
-    a.v = static_cast<const __nv_bfloat16 *>(x.sep ? x.vg : x.v);
+    // global-column rows come from kg / vg with separate projections or a row list
+    const bool gsrc = x.sep || x.gcol_list_rows;
+    a.k = static_cast<const __nv_bfloat16 *>(gsrc ? x.kg : x.k);
+    a.v = static_cast<const __nv_bfloat16 *>(gsrc ? x.vg : x.v);
     for (int i = 0; i < 3; ++i) {
-        a.k_st[i] = x.sep ? x.kg_st[i] : x.k_st[i];
-        a.v_st[i] = x.sep ? x.vg_st[i] : x.v_st[i];
+        a.k_st[i] = gsrc ? x.kg_st[i] : x.k_st[i];
+        a.v_st[i] = gsrc ? x.vg_st[i] : x.v_st[i];
         a.o_st[i] = x.o_st[i];
         a.lse_st[i] = x.lse_st[i];
     }

@@ -75,14 +75,21 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 }
 
 // Key index x of sequence b (0 <= x < Tk = W-1+C): x < W-1 is history position
-// p0 - (W-1) + x, read from its ring slot when the cache holds it; x >= W-1 is chunk
-// token x - (W-1).  Absent history rows are written as zeros and lie below kmin[b].
+// p0 - (W-1) + x, read from its slot (slot rule with n_sink sinks) when the cache holds
+// it; x >= W-1 is chunk token x - (W-1).  Absent history rows are written as zeros and
+// lie below kmin[b].  After the B*Tk*H_kv rows come the B*n_sink*H_kv sink rows: sink
+// position s from its cache slot when s < p0, from the chunk when it lies in the
+// chunk, else zeros (no query of this chunk reaches it).
 template <int D>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
     constexpr int P = 2 * D / 8;
     const int Tk = a.W - 1 + a.C;
-    const int64_t total = static_cast<int64_t>(a.B) * Tk * a.H_kv * P;
+    const int64_t rows_hist = static_cast<int64_t>(a.B) * Tk * a.H_kv;
+    const int64_t total = (rows_hist + static_cast<int64_t>(a.B) * a.n_sink * a.H_kv) * P;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int R = a.n_slots - a.n_sink;  // ring slots
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < a.n_sink; i += blockDim.x) a.sink_idx[i] = i;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
          base += kUnroll * stride) {
         uint4 val[kUnroll];
@@ -94,35 +101,58 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
             if (f >= total) continue;
             const int c = static_cast<int>(f % P);
             const int64_t x = f / P;
-            const int kvh = static_cast<int>(x % a.H_kv);
-            const int64_t bx = x / a.H_kv;
-            const int xx = static_cast<int>(bx % Tk);
-            const int b = static_cast<int>(bx / Tk);
-            const int64_t p0 = __ldg(a.p0 + b);
-            const int64_t have =
-                p0 < 0 ? 0 : min(min(p0, static_cast<int64_t>(a.n_slots)), static_cast<int64_t>(a.W - 1));
-            if (xx == 0 && kvh == 0 && c == 0) {
-                a.kmin[b] = static_cast<int32_t>(a.W - 1 - have);
-                if (p0 < 0) atomicOr(&g_cache_err, kErrBadPosition);
-            }
             const bool is_v = c >= P / 2;
             const int pc = is_v ? c - P / 2 : c;
             val[u] = make_uint4(0, 0, 0, 0);
-            if (xx >= a.W - 1) {
-                const int64_t src = ((static_cast<int64_t>(b) * a.C + (xx - (a.W - 1))) * a.H_kv + kvh) * D;
-                val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
-            } else if (xx >= a.W - 1 - have) {
-                const int64_t p = p0 - (a.W - 1) + xx;
-                const int64_t slot = p % a.n_slots;
-                if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
-                    const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
-                    val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
-                } else if (kvh == 0 && c == 0) {
-                    atomicOr(&g_cache_err, kErrCacheMismatch);
+            if (x < rows_hist) {
+                const int kvh = static_cast<int>(x % a.H_kv);
+                const int64_t bx = x / a.H_kv;
+                const int xx = static_cast<int>(bx % Tk);
+                const int b = static_cast<int>(bx / Tk);
+                const int64_t p0 = __ldg(a.p0 + b);
+                // history positions present right before p0 (a sink cache's ring covers the window)
+                const int64_t ring = a.n_sink == 0 ? a.n_slots : a.W - 1;
+                const int64_t have = p0 < 0 ? 0 : min(min(p0, ring), static_cast<int64_t>(a.W - 1));
+                if (xx == 0 && kvh == 0 && c == 0) {
+                    a.kmin[b] = static_cast<int32_t>(a.W - 1 - have);
+                    if (p0 < 0) atomicOr(&g_cache_err, kErrBadPosition);
                 }
+                if (xx >= a.W - 1) {
+                    const int64_t src = ((static_cast<int64_t>(b) * a.C + (xx - (a.W - 1))) * a.H_kv + kvh) * D;
+                    val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
+                } else if (xx >= a.W - 1 - have) {
+                    const int64_t p = p0 - (a.W - 1) + xx;
+                    const int64_t slot = p < a.n_sink ? p : a.n_sink + (p - a.n_sink) % R;
+                    if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
+                        const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
+                        val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
+                    } else if (kvh == 0 && c == 0) {
+                        atomicOr(&g_cache_err, kErrCacheMismatch);
+                    }
+                }
+                const int64_t dsto = ((static_cast<int64_t>(b) * Tk + xx) * a.H_kv + kvh) * D;
+                dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vl : a.kl) + dsto) + pc;
+            } else {
+                const int64_t y = x - rows_hist;  // (b, s, kvh)
+                const int kvh = static_cast<int>(y % a.H_kv);
+                const int64_t bs = y / a.H_kv;
+                const int sidx = static_cast<int>(bs % a.n_sink);
+                const int b = static_cast<int>(bs / a.n_sink);
+                const int64_t p0 = __ldg(a.p0 + b);
+                if (sidx < p0) {
+                    if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + sidx) == sidx) {
+                        const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + sidx) * D;
+                        val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
+                    } else if (kvh == 0 && c == 0) {
+                        atomicOr(&g_cache_err, kErrCacheMismatch);
+                    }
+                } else if (sidx < p0 + a.C) {
+                    const int64_t src = ((static_cast<int64_t>(b) * a.C + (sidx - p0)) * a.H_kv + kvh) * D;
+                    val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
+                }
+                const int64_t dsto = ((static_cast<int64_t>(b) * a.n_sink + sidx) * a.H_kv + kvh) * D;
+                dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vs : a.ks) + dsto) + pc;
             }
-            const int64_t dsto = ((static_cast<int64_t>(b) * Tk + xx) * a.H_kv + kvh) * D;
-            dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vl : a.kl) + dsto) + pc;
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
@@ -162,7 +192,7 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s) {
-    const int64_t pieces = static_cast<int64_t>(a.B) * (a.W - 1 + a.C) * a.H_kv * (2 * a.D / 8);
+    const int64_t pieces = static_cast<int64_t>(a.B) * (a.W - 1 + a.C + a.n_sink) * a.H_kv * (2 * a.D / 8);
     switch (a.D) {
         case 64: gather_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
         case 128: gather_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;

@@ -116,6 +116,10 @@ struct BandArgs {
     // at key index t + q_off, keys below kmin[b] absent (kmin: device [B] or nullptr).
     int Tk, q_off;
     const int32_t *kmin;
+    // Chunked prefill with sinks: key index q_off of sequence b is position p0[b] (global
+    // positions are then true positions); global-column rows are kg/vg rows in list order.
+    const int32_t *p0;
+    bool gcol_list_rows;
 };
 cudaError_t launch_band(const BandArgs &a, cudaStream_t s);
 
@@ -132,16 +136,19 @@ struct AppendArgs {
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s);
 
 // Window history of a chunk in position order, then the chunk: kl/vl [B, W-1+C, H_kv, D]
-// and kmin[b], the first key index present (ring without sinks: slot p mod n_slots).
+// and kmin[b], the first key index present.  With n_sink pinned sinks also their rows,
+// ks/vs [B, n_sink, H_kv, D] (from the cache, or from the chunk for sinks inside it).
 struct GatherArgs {
     const uint16_t *kc, *vc;
     const int32_t *slot_pos;
-    int B, H_kv, D, n_slots;
+    int B, H_kv, D, n_slots, n_sink;
     const uint16_t *kn, *vn;  // [B, C, H_kv, D]
     int C, W;
     const int32_t *p0;
     uint16_t *kl, *vl;
     int32_t *kmin;
+    uint16_t *ks, *vs;
+    int32_t *sink_idx;  // [n_sink] positions 0 .. n_sink-1 (the band kernel's column list)
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
 unsigned int cache_read_clear_error();  // bit 0: bad position, bit 1: cache mismatch

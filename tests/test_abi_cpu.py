@@ -158,7 +158,7 @@ def _valid_chunk():
     p = swa.SwaChunkParams()
     p.q = p.k_new = p.v_new = p.p0 = p.o = p.lse = 0x10000
     p.B, p.C, p.H_q, p.H_kv, p.d_h = 2, 64, 8, 2, 128
-    p.window, p.scale = 128, 0.1
+    p.window, p.scale = 256, 0.1
     return p
 
 
@@ -198,7 +198,8 @@ def test_decode_append_rejects(lib):
     (lambda p, c: setattr(p, "C", 0), 1),
     (lambda p, c: setattr(p, "B", 3), 1),           # cache of 2 sequences
     (lambda p, c: setattr(p, "d_h", 64), 1),        # cache head dim 128
-    (lambda p, c: setattr(c, "n_sink", 4), 2),      # sink caches not taken here
+    (lambda p, c: setattr(c, "n_sink", 4), 2),      # a sink cache whose ring (252) is shorter than window-1 (255)
+    (lambda p, c: (setattr(c, "n_sink", 200), setattr(c, "n_slots", 600)), 2),  # more than 128 sinks
     (lambda p, c: setattr(p, "q", 0x10004), 2),
 ])
 def test_prefill_chunk_rejects(lib, mutate, status):
@@ -212,7 +213,7 @@ def test_prefill_chunk_workspace(lib):
     p, c = _valid_chunk(), _valid_cache()
     need = lib.swa_prefill_chunk_workspace_size(ctypes.byref(p), ctypes.byref(c))
     # gathered keys and values: B * (W - 1 + C) * H_kv * d_h bf16 each, plus kmin
-    assert need >= 2 * 2 * (128 - 1 + 64) * 2 * 128 * 2
+    assert need >= 2 * 2 * (256 - 1 + 64) * 2 * 128 * 2
     assert lib.swa_prefill_chunk(ctypes.byref(p), ctypes.byref(c), None, 0, None) == 5
 
 

@@ -137,6 +137,49 @@ def test_prefill_chunk(case):
     np.testing.assert_array_equal(_bits(vd), vc2)
 
 
+CHUNK_SINKS = [
+    # B, C, Hq, Hkv, d, W, n_sink, ring slots, p0 per sequence
+    (2, 100, 4, 2, 128, 64, 4, 74, [0, 300]),      # p0 = 0: the sinks are inside the chunk
+    (1, 200, 8, 2, 64, 100, 2, 99, [3]),
+    (2, 64, 4, 1, 256, 32, 1, 40, [1000, 7]),
+    (1, 300, 4, 2, 128, 64, 128, 64, [500]),       # the largest sink count
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_SINKS, ids=[f"C{c[1]}-d{c[4]}-W{c[5]}-ns{c[6]}" for c in CHUNK_SINKS])
+def test_prefill_chunk_with_sinks(case):
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    B, C, Hq, Hkv, d, W, ns, R, p0 = case
+    p0 = np.array(p0, dtype=np.int32)
+    S = ns + R
+    kc, vc, pos = _empty_cache(960 + C, B, Hkv, S, d)
+    Tm = int(p0.max())
+    kh = I.normal_bf16(961 + C, (B, max(Tm, 1), Hkv, d))
+    vh = I.normal_bf16(962 + C, (B, max(Tm, 1), Hkv, d))
+    for b in range(B):
+        if p0[b]:
+            kb, vb, pb = oracle.cache_append(kc[b:b + 1], vc[b:b + 1], pos[b:b + 1], kh[b:b + 1, :p0[b]],
+                                             vh[b:b + 1, :p0[b]], [0], n_sink=ns)
+            kc[b], vc[b], pos[b] = kb[0], vb[0], pb[0]
+    q = I.normal_bf16(963 + C, (B, C, Hq, d))
+    kn = I.normal_bf16(964 + C, (B, C, Hkv, d))
+    vn = I.normal_bf16(965 + C, (B, C, Hkv, d))
+    kd, vd, pd = to_dev(kc), to_dev(vc), i32_dev(pos)
+    o, lse, cnt = swa.swa_prefill_chunk(to_dev(q), to_dev(kn), to_dev(vn), kd, vd, pd, i32_dev(p0), W, d ** -0.5,
+                                        append=True, want_counts=True, n_sink=ns)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o_ref, lse_ref, cnt_ref = oracle.chunk(q, kn, vn, kc, vc, pos, p0, W, d ** -0.5, n_sink=ns)
+    assert_parity(to_host_f64(o).transpose(0, 2, 1, 3), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref,
+                  cnt_ref, str(case))
+    kc2, vc2, pos2 = oracle.cache_append(kc, vc, pos, kn, vn, p0, n_sink=ns)
+    np.testing.assert_array_equal(pd.cpu().numpy(), pos2)
+    np.testing.assert_array_equal(_bits(kd), kc2)
+    np.testing.assert_array_equal(_bits(vd), vc2)
+
+
 def test_prefill_chunk_reports_missing_history():
     import torch
     import sliding_window_attention_swa_gb300 as swa
