@@ -55,7 +55,8 @@ struct StageHdr {
 template <int D>
 struct StreamCfg {
     static constexpr int STAGE = 2 * CH * D * 2;        // K + V of one chunk
-    static constexpr int CBUF = 4 * kSplitRows * D * 4;  // combine buffer [4 warps][16 rows][D] fp32
+    static constexpr int CROW = D + 8;  // padded row: float2 stores of 4 rows per half-warp hit distinct banks
+    static constexpr int CBUF = 4 * kSplitRows * CROW * 4;  // combine buffer [4 warps][16 rows][CROW] fp32
     static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
     static constexpr int NST_RAW = (232448 / CTAS_PER_SM - 2048 - CBUF) / STAGE;
     static constexpr int NST = NST_RAW > 8 ? 8 : NST_RAW;
@@ -414,13 +415,13 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 if (r0 < rows) {
 #pragma unroll
                     for (int n = 0; n < D / 8; ++n)
-                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r0) * D + 8 * n + kq) =
+                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r0) * C::CROW + 8 * n + kq) =
                             make_float2(acc[n][0], acc[n][1]);
                 }
                 if (r1 < rows) {
 #pragma unroll
                     for (int n = 0; n < D / 8; ++n)
-                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r1) * D + 8 * n + kq) =
+                        *reinterpret_cast<float2 *>(cbuf + (w * kSplitRows + r1) * C::CROW + 8 * n + kq) =
                             make_float2(acc[n][2], acc[n][3]);
                 }
                 __syncwarp();
@@ -442,7 +443,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 #pragma unroll
                     for (int ww = 0; ww < 4; ++ww) {
                         const float f = mw == -INFINITY ? 0.f : ex2(red_m[ww * kSplitRows + r] - mw);
-                        s += cbuf[(ww * kSplitRows + r) * D + d] * f;
+                        s += cbuf[(ww * kSplitRows + r) * C::CROW + d] * f;
                         L += red_l[ww * kSplitRows + r] * f;
                     }
                     const int64_t row = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits + split;
