@@ -41,7 +41,7 @@ def headline_config(world: int) -> dict:
     return {"workload": c.name, "B": c.B, "T": c.T, "H_q": c.Hq, "H_kv": c.Hkv, "d_h": c.d,
             "window": c.window_left + 1, "causal": True,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "flushed (256 MB write) before every timed step", "flops_per_step": prefill_flops(c)}
+            "l2": "flushed before every timed step (256 MB write, then 256 MB read: cold, clean L2)", "flops_per_step": prefill_flops(c)}
 KERNELS = {"band": "band_fwd_kernel", "split": "stream_attn_kernel", "merge": "merge_kernel"}
 
 
@@ -195,10 +195,29 @@ class _Null:
         return False
 
 
+class L2Flush:
+    """Leaves L2 cold before a timed call: a 256 MB write evicts whatever the previous
+    call left there, then a 256 MB read evicts the written (dirty) lines in turn, so
+    their write-back to HBM happens here and not inside the next call's events."""
+
+    def __init__(self, device):
+        import torch
+
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+        self.out = torch.empty((), dtype=torch.int64, device=device)
+
+    def zero_(self):
+        import torch
+
+        self.w.zero_()
+        torch.amax(self.r, dim=0, out=self.out)
+
+
 def timed_steps(fn, steps: int, warmup: int, flush, stream, sampler=None):
     """W untimed warm-up calls, then K calls each bracketed by CUDA events on `stream`
-    with an L2 flush (a 256 MB write) before each call, outside its events.  The
-    optional clock sampler runs only around the K timed calls."""
+    with an L2 flush (L2Flush: a 256 MB write, then a 256 MB read) before each call,
+    outside its events.  The optional clock sampler runs only around the K timed calls."""
     import torch
 
     for _ in range(warmup):
@@ -604,7 +623,7 @@ def main():
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     only = set(args.only.split(",")) if args.only else {"mistral", "decode", "gemma", "longformer", "variants",
                                                          "cache"}
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     def barrier():
         if world > 1:

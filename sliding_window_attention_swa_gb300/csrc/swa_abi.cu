@@ -152,6 +152,18 @@ swa_status workspace_ok(void *ws, size_t have, size_t need) {
 // Global rows (attending to every key) exist only for SWA_GLOBAL_FULL.
 bool has_global_rows(const swa_fwd_params *p) { return p->n_global > 0 && p->global_mode == SWA_GLOBAL_FULL; }
 
+// Split size and count of the global-row pass: its items are (batch, kv head, query
+// block) groups times the splits of T, sized to the persistent grid.
+int global_row_split_size(const swa_fwd_params *p) {
+    const int qpc = swa::split_q_per_cta(p->H_q / p->H_kv);
+    const long long pairs = static_cast<long long>(p->B) * p->H_kv * ((p->n_global + qpc - 1) / qpc);
+    return swa::split_size_for_grid(p->T, pairs, swa::split_grid(p->d_h));
+}
+int global_row_splits(const swa_fwd_params *p) {
+    const int sz = global_row_split_size(p);
+    return (p->T + sz - 1) / sz;
+}
+
 // Band launches of swa_fwd.  A dilated head attends, within each residue class
 // t = r (mod d), to the ordinary band of that subsequence (keys t + k*d), so every
 // (dilation, residue) pair is one launch over strided views of q, k, v, o, lse and
@@ -223,7 +235,7 @@ swa_status swa::validate_decode(const swa_decode_params *p) { return decode_chec
 bool swa::record_cuda_failure(cudaError_t e) { return failed(e); }
 
 size_t swa::decode_workspace_bytes(const swa_decode_params *p) {
-    return split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, p->W);
+    return split_workspace_bytes(p->B, 1, p->H_q, p->H_kv, p->d_h, split_count(p->W));
 }
 
 cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s, const void *k_new,
@@ -255,7 +267,7 @@ cudaError_t swa::run_decode(const swa_decode_params *p, void *ws, cudaStream_t s
     sa.slots_per_split = split_size(p->W);
     sa.n_splits = split_count(p->W);
     sa.q_per_cta = split_q_per_cta(p->H_q / p->H_kv);
-    split_carve(ws, p->B, 1, p->H_q, p->H_kv, p->d_h, p->W, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
+    split_carve(ws, p->B, 1, p->H_q, p->d_h, sa.n_splits, &sa.ws_ml, &sa.ws_acc, &sa.ws_cnt);
     sa.k_new = static_cast<const uint16_t *>(k_new);
     sa.v_new = static_cast<const uint16_t *>(v_new);
     sa.slot_pos_w = const_cast<int32_t *>(p->slot_pos);
@@ -309,7 +321,7 @@ const char *swa_status_string(swa_status s) {
 
 size_t swa_fwd_workspace_size(const swa_fwd_params *p) {
     if (fwd_check(p) != SWA_OK || !has_global_rows(p)) return 0;
-    return swa::split_workspace_bytes(p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T);
+    return swa::split_workspace_bytes(p->B, p->n_global, p->H_q, p->H_kv, p->d_h, global_row_splits(p));
 }
 
 swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_bytes, swa_stream_t stream) {
@@ -389,10 +401,10 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         sa.W = p->T;
         sa.n_sink = 0;
         sa.scale_log2 = scale_log2;
-        sa.slots_per_split = swa::split_size(p->T);
-        sa.n_splits = swa::split_count(p->T);
+        sa.slots_per_split = global_row_split_size(p);
+        sa.n_splits = (p->T + sa.slots_per_split - 1) / sa.slots_per_split;
         sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
-        swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->H_kv, p->d_h, p->T, &sa.ws_ml, &sa.ws_acc,
+        swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->d_h, sa.n_splits, &sa.ws_ml, &sa.ws_acc,
                          &sa.ws_cnt);
         if (failed(swa::launch_split(sa, s))) return SWA_ERR_CUDA;
         swa::MergeArgs ma{};

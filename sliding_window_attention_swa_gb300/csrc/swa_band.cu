@@ -38,6 +38,7 @@
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and MMAs, frees TMEM and returns.
 #include <cfloat>
+#include <climits>
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -100,6 +101,7 @@ struct BandKernelArgs {
     // positions, and with gcol_list_rows their K/V rows are the k/v rows in list order
     const int32_t *p0;
     int gcol_list_rows;
+    int gcol_hi;  // global positions at or above gcol_hi are not keys (Tk; no bound with a row list)
     int wl, wr;
     float scale_log2;
     const int32_t *global_idx;
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         // projections every global key is scored here
                         const bool outside =
                             (gs < lo_abs + w.pos_off) | ((gs > hi_abs + w.pos_off) & !a.sink);
-                        const bool valid = a.gcol_list_rows ? gs >= 0 : (gs >= 0) & (gs < a.Tk);
+                        const bool valid = (gs >= 0) & (gs < a.gcol_hi);
                         const bool al = valid & (outside | (a.sep != 0));
                         cnt4[c & 3] += al ? 1 : 0;
                         x[c] = al ? x[c] : -INFINITY;
@@ -786,6 +788,7 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.kmin = x.kmin;
     a.p0 = x.p0;
     a.gcol_list_rows = x.gcol_list_rows ? 1 : 0;
+    a.gcol_hi = x.gcol_list_rows ? INT_MAX : Tk;
     a.H_q = x.H_q;
     a.H_kv = x.H_kv;
     a.G = G;

@@ -71,16 +71,39 @@ inline int split_size(int n_slots) {
     const int per = (n_slots + ns - 1) / ns;
     return (per + kSplitChunk - 1) / kSplitChunk * kSplitChunk;
 }
-inline size_t split_workspace_bytes(int B, int NQ, int H_q, int H_kv, int D, int n_slots) {
-    const size_t ns = static_cast<size_t>(split_count(n_slots));
+// Slots per split for a pass whose items are `pairs` (batch, kv head, query block)
+// groups times the splits of n_slots, dealt round-robin to `grid` persistent CTAs.
+// Among whole-chunk splits from 256 slots up to kSlotsPerSplit (each balanced like
+// split_size), take the one that finishes in the fewest slot-times, counting about
+// 96 slots of fixed cost per item (its end-of-item combine).  A pass of few groups
+// (the global rows of a short sequence) gets smaller splits so the last wave of items
+// is not left half empty.
+inline int split_size_for_grid(int n_slots, long long pairs, int grid) {
+    const int ns_min = split_count(n_slots);
+    const int ns_max = ns_min > (n_slots + 255) / 256 ? ns_min : (n_slots + 255) / 256;
+    int best = split_size(n_slots);
+    long long best_t = -1;
+    for (int ns = ns_min; ns <= ns_max; ++ns) {
+        const int per = (n_slots + ns - 1) / ns;
+        const int sz = (per + kSplitChunk - 1) / kSplitChunk * kSplitChunk;
+        if (sz > kSlotsPerSplit) continue;
+        const long long items = pairs * ((n_slots + sz - 1) / sz);
+        const long long t = (items + grid - 1) / grid * (sz + 96);
+        if (best_t < 0 || t < best_t) {
+            best_t = t;
+            best = sz;
+        }
+    }
+    return best;
+}
+// Workspace of a split pass with ns splits: ml, acc and cnt, each 256-byte aligned.
+inline size_t split_workspace_bytes(int B, int NQ, int H_q, int H_kv, int D, int ns) {
     const size_t rows = static_cast<size_t>(B) * NQ * H_q * ns;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     return up(rows * 2 * sizeof(float)) + up(rows * D * sizeof(float)) +
            up(static_cast<size_t>(B) * H_kv * ns * sizeof(int32_t));
 }
-inline void split_carve(void *ws, int B, int NQ, int H_q, int H_kv, int D, int n_slots, float **ml, float **acc,
-                        int32_t **cnt) {
-    const size_t ns = static_cast<size_t>(split_count(n_slots));
+inline void split_carve(void *ws, int B, int NQ, int H_q, int D, int ns, float **ml, float **acc, int32_t **cnt) {
     const size_t rows = static_cast<size_t>(B) * NQ * H_q * ns;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     char *p = static_cast<char *>(ws);
@@ -91,6 +114,8 @@ inline void split_carve(void *ws, int B, int NQ, int H_q, int H_kv, int D, int n
     *cnt = reinterpret_cast<int32_t *>(p);
 }
 
+// Persistent CTAs of the split pass at head dim D on the current device.
+int split_grid(int D);
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 unsigned int split_read_clear_error();

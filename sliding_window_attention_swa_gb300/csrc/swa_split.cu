@@ -127,6 +127,9 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
     }
     __syncthreads();
     volatile int *abort = &abort_flag;
+    // the merge grid may be scheduled from here on: its blocks wait (griddepcontrol.wait)
+    // for this grid to complete before they read the partials
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ============================ producer ============================
@@ -464,6 +467,9 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 }
 
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
+    // launched as a programmatic dependent of the split pass: wait for that grid's
+    // completion (and its writes) before reading the partials
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int qs = blockIdx.x / a.H_q, h = blockIdx.x % a.H_q, b = blockIdx.y;
     const int group = a.H_q / a.H_kv, kvh = h / group;
     const int64_t base = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits;
@@ -571,6 +577,8 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
 
 }  // namespace
 
+int split_grid(int D) { return sm_count() * (D <= 128 ? StreamCfg<128>::CTAS_PER_SM : StreamCfg<256>::CTAS_PER_SM); }
+
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t s) {
     switch (a.D) {
         case 64: return launch_stream_d<64>(a, s);
@@ -581,9 +589,19 @@ cudaError_t launch_split(const SplitArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s) {
-    dim3 grid(a.NQ * a.H_q, a.B);
-    merge_kernel<<<grid, 128, 0, s>>>(a);
-    return cudaGetLastError();
+    // programmatic dependent launch: the merge grid is launched while the split pass
+    // before it on the stream drains, instead of after it
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.NQ * a.H_q, a.B);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 unsigned int split_read_clear_error() {
