@@ -406,6 +406,7 @@ swa_status swa_fwd(const swa_fwd_params *p, void *workspace, size_t workspace_by
         sa.q_per_cta = swa::split_q_per_cta(p->H_q / p->H_kv);
         swa::split_carve(workspace, p->B, p->n_global, p->H_q, p->d_h, sa.n_splits, &sa.ws_ml, &sa.ws_acc,
                          &sa.ws_cnt);
+        sa.after_band = 1;
         if (failed(swa::launch_split(sa, s))) return SWA_ERR_CUDA;
         swa::MergeArgs ma{};
         ma.ws_ml = sa.ws_ml;

@@ -52,6 +52,7 @@ namespace {
 __device__ unsigned int g_band_err = 0;
 
 constexpr int BM = 128;              // query rows per tile (TMEM lanes)
+constexpr int kNarrow = 32;          // width of a narrow global-column tile
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 template <int D>
@@ -116,6 +117,9 @@ struct BandKernelArgs {
     float *lse;
     int32_t *counts;
     int64_t lse_st[3];
+    // at most kNarrow global positions: their one column tile is kNarrow keys wide (S with
+    // N = kNarrow, P V with K = kNarrow, a kNarrow-column softmax) instead of BN
+    int gcol_narrow;
 };
 
 // Index of the first entry >= k0 of the sorted list g[0..n) (n if none).
@@ -226,6 +230,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     volatile int *abort = &abort_flag;
+    // a dependent grid launched behind this one (the global-row pass, only with global
+    // positions) reads none of its outputs: it may take SMs as soon as this grid's CTAs
+    // leave them
+    if constexpr (kGlob) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ============================ K/V producer ============================
@@ -258,7 +266,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     const __nv_bfloat16 *src = is_v ? a.v : a.k;
                     const int64_t *st = is_v ? a.v_st : a.k_st;
                     constexpr int kPieces = D / 8;
-                    for (int idx = lane; idx < BN * kPieces; idx += 32) {
+                    const int rows = a.gcol_narrow ? kNarrow : BN;  // rows the MMAs read
+                    for (int idx = lane; idx < rows * kPieces; idx += 32) {
                         const int r = idx / kPieces, pc = idx % kPieces;
                         const int gi = g0 + r;
                         int srow = -1;
@@ -329,12 +338,13 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idS_narrow = idesc_bf16_f32(BM, kNarrow, false, false);
             constexpr uint32_t idPV = idesc_bf16_f32(BM, D, false, true);
             bool ok = true;
             int J = 0;  // key tiles of this CTA's previous units
             int k = 0;  // units of this CTA so far
             // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
-            auto mma_s = [&](int slot, int qt, int jg, bool wait_k) -> bool {
+            auto mma_s = [&](int slot, int qt, int jg, bool wait_k, bool narrow = false) -> bool {
                 const int fi = 2 * jg, s = fi % NSLOT;
                 if (wait_k && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
@@ -343,12 +353,15 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ad = smem_desc(qb + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
                     const uint64_t bd = smem_desc(kb + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    tc_mma_ss(tmem + C::tm_s(slot), ad, bd, idS, kk > 0 ? 1u : 0u);
+                    uint32_t id = idS;
+                    if constexpr (kGlob) id = narrow ? idS_narrow : idS;
+                    tc_mma_ss(tmem + C::tm_s(slot), ad, bd, id, kk > 0 ? 1u : 0u);
                 }
                 return true;
             };
             // O_tile (+)= P(slot) V of global tile index jg; `first` starts a fresh O.
-            auto mma_pv = [&](int slot, int otile, int jg, uint32_t p_parity, bool wait_v, bool first) -> bool {
+            auto mma_pv = [&](int slot, int otile, int jg, uint32_t p_parity, bool wait_v, bool first,
+                              bool narrow = false) -> bool {
                 const int fi = 2 * jg + 1, s = fi % NSLOT;
                 if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
                 if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
@@ -358,6 +371,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const uint32_t vb = sRing + s * C::TBYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
+                    if constexpr (kGlob) {
+                        if (narrow && kk >= kNarrow / 16) break;
+                    }
                     const uint64_t bd = smem_desc(vb + kk * 2048, BN * 128, 1024, kSwizzle128B);
                     tc_mma_ts(tmem + C::tm_o(otile), tmem + C::tm_s(slot) + kk * 8, bd, idPV,
                               (!first || kk > 0) ? 1u : 0u);
@@ -369,16 +385,19 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
             for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
                 const int n = unit_of<NQT, BN>(u, a).n_tiles;
+                // tile jj of the unit is the narrow global-column tile
+                const int nb = kGlob ? unit_of<NQT, BN>(u, a).n_band : n;
+                auto narrow = [&](int jj) { return kGlob && a.gcol_narrow && jj >= nb; };
                 // each query tile is waited for just before its first S MMA
                 ok = mbar_wait(bar_qf(0), k & 1, abort, &g_band_err);
                 if (!ok) break;
                 if constexpr (NQT == 2) {
-                    ok = mma_s(0, 0, J, true);
+                    ok = mma_s(0, 0, J, true, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(0));
                         ok = mbar_wait(bar_qf(1), k & 1, abort, &g_band_err);
                     }
-                    if (ok) ok = mma_s(1, 1, J, false);
+                    if (ok) ok = mma_s(1, 1, J, false, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(1));
                         tc_commit(bar_empty(kslot(J)));
@@ -386,20 +405,20 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
                     for (int j = 0; j < n && ok; ++j) {
                         const int jg = J + j;
-                        ok = mma_pv(0, 0, jg, jg & 1, true, j == 0);
+                        ok = mma_pv(0, 0, jg, jg & 1, true, j == 0, narrow(j));
                         if (!ok) break;
                         if (j + 1 < n) {
-                            ok = mma_s(0, 0, jg + 1, true);
+                            ok = mma_s(0, 0, jg + 1, true, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf(0));
                         } else {
                             tc_commit(bar_od(0));
                         }
-                        ok = mma_pv(1, 1, jg, jg & 1, false, j == 0);
+                        ok = mma_pv(1, 1, jg, jg & 1, false, j == 0, narrow(j));
                         if (!ok) break;
                         tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 < n) {
-                            ok = mma_s(1, 1, jg + 1, false);
+                            ok = mma_s(1, 1, jg + 1, false, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf(1));
                             tc_commit(bar_empty(kslot(jg + 1)));
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         }
                     }
                 } else {
-                    ok = mma_s(J & 1, 0, J, true);
+                    ok = mma_s(J & 1, 0, J, true, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(J & 1));
                         tc_commit(bar_empty(kslot(J)));
@@ -418,12 +437,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         const int jg = J + j;
                         if (j + 1 < n) {
                             // slot (jg+1)&1 last held P of tile jg-1, consumed by its P V issued earlier
-                            ok = mma_s((jg + 1) & 1, 0, jg + 1, true);
+                            ok = mma_s((jg + 1) & 1, 0, jg + 1, true, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf((jg + 1) & 1));
                             tc_commit(bar_empty(kslot(jg + 1)));
                         }
-                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0);
+                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0, narrow(j));
                         if (!ok) break;
                         tc_commit(bar_pv(jg & 1));
                         tc_commit(bar_empty(vslot(jg)));
@@ -475,6 +494,94 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_addr + C::tm_s(slot);
+                if constexpr (kGlob) {
+                    if (a.gcol_narrow && j >= w.n_band) {
+                        // the unit's one global-column tile, at most kNarrow keys wide: the
+                        // staged positions left of the row's band are a prefix [0, nl) of the
+                        // sorted list and those right of it a suffix [nr, n); sinks keep only
+                        // the prefix, separate projections keep every column
+                        float xn[kNarrow];
+                        {
+                            uint32_t raw[32];
+                            tmem_ld32(s_addr, raw);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < kNarrow; ++e) xn[e] = __uint_as_float(raw[e]);
+                        }
+                        const int n = a.n_global;
+                        const int lo_pos = lo_abs + w.pos_off, hi_pos = hi_abs + w.pos_off;
+                        int nl = 0, nr = 0;
+#pragma unroll
+                        for (int step = kNarrow; step >= 1; step >>= 1) {
+                            if (nl + step <= n && gpos[nl + step - 1] < lo_pos) nl += step;
+                            if (nr + step <= n && gpos[nr + step - 1] <= hi_pos) nr += step;
+                        }
+                        if (a.sink) nr = n;
+                        if (a.sep) nl = nr = n;
+                        count += nl + (n - nr);
+#pragma unroll
+                        for (int c = 0; c < kNarrow; ++c)
+                            xn[c] = (c < nl) | ((c >= nr) & (c < n)) ? xn[c] : -INFINITY;
+                        float mx8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            mx8[i] = fmaxf(fmax3(xn[i], xn[8 + i], xn[16 + i]), xn[24 + i]);
+                        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                               fmaxf(mx8[6], mx8[7]));
+                        const float mt = mx * a.scale_log2;
+                        const bool need = mt > m + kRescaleTau;
+                        const float mu = need ? mt : m;
+                        const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
+                        if (__any_sync(0xffffffffu, need) && j > 0) {
+                            // O holds P V of tiles 0 .. j-1 of this unit and must be complete.
+                            if constexpr (NQT == 1) {
+                                if (!warp_wait(bar_pv((jg - 1) & 1), ((jg - 1) >> 1) & 1, abort)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
+#pragma unroll 1
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t ov[32];
+                                tmem_ld32(o_addr + c * 32, ov);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                                tmem_st32(o_addr + c * 32, ov);
+                            }
+                        }
+                        m = mu;
+                        const float msub = mu == -INFINITY ? 0.f : mu;
+                        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-msub, -msub);
+                        uint64_t rs2[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) rs2[i] = f2_pack(0.f, 0.f);
+                        uint32_t pk[kNarrow / 2];
+#pragma unroll
+                        for (int e = 0; e < kNarrow / 2; ++e) {
+                            float t0, t1;
+                            f2_unpack(f2_fma(f2_pack(xn[2 * e], xn[2 * e + 1]), sc2, nm2), t0, t1);
+                            const float p0 = ex2(t0), p1 = ex2(t1);
+                            rs2[e & 3] = f2_add(rs2[e & 3], f2_pack(p0, p1));
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_addr, pk);
+                        tc_wait_st();
+                        float rsum;
+                        {
+                            const uint64_t r01 = f2_add(rs2[0], rs2[1]), r23 = f2_add(rs2[2], rs2[3]);
+                            float lo, hi;
+                            f2_unpack(f2_add(r01, r23), lo, hi);
+                            rsum = lo + hi;
+                        }
+                        l = l * alpha + rsum;
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_pf(slot));
+                        continue;
+                    }
+                }
                 float x[BN];
                 {
                     uint32_t raw[BN / 32][32];
@@ -802,6 +909,7 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.n_global = x.n_global;
     a.sink = x.gmode == SWA_GLOBAL_SINK ? 1 : 0;
     a.sep = x.sep ? 1 : 0;
+    a.gcol_narrow = glob && x.n_global <= kNarrow ? 1 : 0;
     // global-column rows come from kg / vg with separate projections or a row list
     const bool gsrc = x.sep || x.gcol_list_rows;
     a.k = static_cast<const __nv_bfloat16 *>(gsrc ? x.kg : x.k);

@@ -40,6 +40,10 @@ struct SplitArgs {
     // slot(q_pos[b]) before it is read (nullptr: none), and slot_pos to update there.
     const uint16_t *k_new, *v_new;
     int32_t *slot_pos_w;
+    // Global rows: launched as a programmatic dependent of the band kernel before it on
+    // the stream (it reads only q/k/v, so it may start on SMs the band kernel has left);
+    // the grid then waits for that kernel before completing.
+    int after_band;
 };
 
 struct MergeArgs {

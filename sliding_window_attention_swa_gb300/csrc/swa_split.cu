@@ -464,6 +464,10 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
             }
         }
     }
+    // After the band kernel of the same call (global rows): complete only once that grid has,
+    // so the merge, which waits for this grid, overwrites the band kernel's rows after it.
+    // (Without a programmatic launch this returns at once.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
@@ -571,8 +575,21 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
     ka.n_items = static_cast<int>(items);
     const int slots = sm_count() * C::CTAS_PER_SM;
     const int grid = static_cast<int>(items < slots ? items : slots);
-    stream_attn_kernel<D><<<grid, kThreads, C::SMEM, s>>>(mk, mv, ka);
-    return cudaGetLastError();
+    if (!a.after_band) {
+        stream_attn_kernel<D><<<grid, kThreads, C::SMEM, s>>>(mk, mv, ka);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stream_attn_kernel<D>, mk, mv, ka);
 }
 
 }  // namespace

@@ -74,6 +74,32 @@ def test_sinks_full_size_mistral():
     assert_parity(o[b, h, tt], lse[b, h, tt], cnt[b, h, tt], o_ref, lse_ref, cnt_ref, "mistral+sinks")
 
 
+# ----------------------------------------------------------------------------- narrow global tile
+# Up to 32 global positions are scored in one 32-key tile (S with N = 32, P V with K = 32,
+# a 32-column softmax); 33 or more take full-width tiles.  Both sides of that boundary,
+# with globals inside and outside the bands, as full globals and as sinks.
+NARROW = [
+    # B, T, Hq, Hkv, d, wl, wr, G, mode
+    (1, 700, 4, 2, 128, 40, 40, list(range(0, 700, 22))[:32], "full"),      # 32: narrow
+    (1, 700, 4, 2, 128, 40, 40, list(range(0, 700, 21))[:33], "full"),      # 33: full width
+    (2, 500, 8, 8, 64, 30, 30, [0, 1, 31, 32, 250, 498, 499], "full"),
+    (1, 400, 4, 2, 256, 50, 0, list(range(32)), "sink"),                   # 32 sinks, d = 256
+    (1, 400, 4, 2, 256, 50, 0, list(range(33)), "sink"),                   # 33 sinks
+    (1, 300, 2, 1, 64, 20, 0, [7], "sink"),
+]
+
+
+@pytest.mark.parametrize("case", NARROW, ids=[f"T{c[1]}-d{c[4]}-g{len(c[7])}-{c[8]}" for c in NARROW])
+def test_narrow_global_tile(case):
+    B, T, Hq, Hkv, d, wl, wr, G, mode = case
+    q, k, v = _inputs(7 * T + d + len(G), B, T, Hq, Hkv, d)
+    scale = d ** -0.5
+    gmode = oracle.GLOBAL_SINK if mode == "sink" else oracle.GLOBAL_FULL
+    o, lse, cnt = _run(q, k, v, wl, wr, scale, G, global_mode=gmode)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, wl, wr, scale, G, gmode=gmode)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, str(case[:7]) + f" g={len(G)} {mode}")
+
+
 # ----------------------------------------------------------------------------- global projections
 SEP = [
     # B, T, Hq, Hkv, d, wl, wr, G
