@@ -21,13 +21,37 @@ constexpr unsigned int kErrCacheMismatch = 2u;  // a slot not holding the positi
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;  // independent 16-byte loads in flight per thread
 
+// Division of 31-bit values by a divisor fixed for the launch, by a multiply-high and a
+// shift (Granlund and Montgomery, "Division by invariant integers using multiplication",
+// 1994): with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1,
+// x / d = (umulhi(x, m) + x) >> s for 0 <= x < 2^31.  The kernels' index arithmetic
+// would otherwise spend more time in 64-bit division than in moving the data.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+FastDiv fast_div(uint32_t d) {
+    uint32_t s = 0;
+    while ((uint64_t{1} << s) < d) ++s;
+    const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << s) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), s};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv &f) { return (__umulhi(x, f.m) + x) >> f.s; }
+
+// Divisors of the two kernels' flat indices.
+struct CopyPlan {
+    FastDiv hkv;   // H_kv
+    FastDiv n;     // tokens per sequence (append: n; gather: W - 1 + C)
+    FastDiv ring;  // ring slots n_slots - n_sink
+    FastDiv sink;  // n_sink (gather)
+};
+
 // Both kernels walk a flat list of 16-byte pieces: piece c of (sequence, token, kv
 // head) x is the c-th of the 2*D/8 pieces of its key row then its value row, so a
 // warp's lanes cover consecutive pieces of the same rows (coalesced).  Each thread
 // issues kUnroll loads before its stores.
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, const CopyPlan pl) {
     constexpr int P = 2 * D / 8;
     const int64_t total = static_cast<int64_t>(a.B) * a.n * a.H_kv * P;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -42,11 +66,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
             const int64_t f = base + u * stride;
             if (f >= total) continue;
             const int c = static_cast<int>(f % P);
-            const int64_t x = f / P;
-            const int kvh = static_cast<int>(x % a.H_kv);
-            const int64_t bi = x / a.H_kv;
-            const int i = static_cast<int>(bi % a.n);
-            const int b = static_cast<int>(bi / a.n);
+            const uint32_t x = static_cast<uint32_t>(f / P);  // < 2^31 rows (checked at launch)
+            const uint32_t bi = fdiv(x, pl.hkv);
+            const int kvh = static_cast<int>(x - bi * pl.hkv.d);
+            const uint32_t bq = fdiv(bi, pl.n);
+            const int i = static_cast<int>(bi - bq * pl.n.d);
+            const int b = static_cast<int>(bq);
             const int64_t p0 = __ldg(a.p0 + b);
             const int64_t p = p0 + i, last = p0 + a.n - 1;
             if (p0 < 0 || last > INT_MAX) {
@@ -58,7 +83,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
                 slot = p;
             } else {
                 if (last - p >= R) continue;  // a later token of this call takes the same ring slot
-                slot = a.n_sink + (p - a.n_sink) % R;
+                const uint32_t pr = static_cast<uint32_t>(p - a.n_sink);
+                slot = a.n_sink + (pr - fdiv(pr, pl.ring) * pl.ring.d);
             }
             const bool is_v = c >= P / 2;
             const int pc = is_v ? c - P / 2 : c;
@@ -81,13 +107,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 // position s from its cache slot when s < p0, from the chunk when it lies in the
 // chunk, else zeros (no query of this chunk reaches it).
 template <int D>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
+__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a, const CopyPlan pl) {
     constexpr int P = 2 * D / 8;
     const int Tk = a.W - 1 + a.C;
     const int64_t rows_hist = static_cast<int64_t>(a.B) * Tk * a.H_kv;
     const int64_t total = (rows_hist + static_cast<int64_t>(a.B) * a.n_sink * a.H_kv) * P;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int R = a.n_slots - a.n_sink;  // ring slots
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < a.n_sink; i += blockDim.x) a.sink_idx[i] = i;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
@@ -105,10 +130,12 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
             const int pc = is_v ? c - P / 2 : c;
             val[u] = make_uint4(0, 0, 0, 0);
             if (x < rows_hist) {
-                const int kvh = static_cast<int>(x % a.H_kv);
-                const int64_t bx = x / a.H_kv;
-                const int xx = static_cast<int>(bx % Tk);
-                const int b = static_cast<int>(bx / Tk);
+                const uint32_t x32 = static_cast<uint32_t>(x);  // < 2^31 rows (checked at launch)
+                const uint32_t bx = fdiv(x32, pl.hkv);
+                const int kvh = static_cast<int>(x32 - bx * pl.hkv.d);
+                const uint32_t bq = fdiv(bx, pl.n);
+                const int xx = static_cast<int>(bx - bq * pl.n.d);
+                const int b = static_cast<int>(bq);
                 const int64_t p0 = __ldg(a.p0 + b);
                 // history positions present right before p0 (a sink cache's ring covers the window)
                 const int64_t ring = a.n_sink == 0 ? a.n_slots : a.W - 1;
@@ -122,7 +149,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
                     val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
                 } else if (xx >= a.W - 1 - have) {
                     const int64_t p = p0 - (a.W - 1) + xx;
-                    const int64_t slot = p < a.n_sink ? p : a.n_sink + (p - a.n_sink) % R;
+                    const uint32_t pr = static_cast<uint32_t>(p - a.n_sink);
+                    const int64_t slot = p < a.n_sink ? p : a.n_sink + (pr - fdiv(pr, pl.ring) * pl.ring.d);
                     if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
                         const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
                         val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
@@ -133,11 +161,12 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a) {
                 const int64_t dsto = ((static_cast<int64_t>(b) * Tk + xx) * a.H_kv + kvh) * D;
                 dst[u] = reinterpret_cast<uint4 *>((is_v ? a.vl : a.kl) + dsto) + pc;
             } else {
-                const int64_t y = x - rows_hist;  // (b, s, kvh)
-                const int kvh = static_cast<int>(y % a.H_kv);
-                const int64_t bs = y / a.H_kv;
-                const int sidx = static_cast<int>(bs % a.n_sink);
-                const int b = static_cast<int>(bs / a.n_sink);
+                const uint32_t y = static_cast<uint32_t>(x - rows_hist);  // (b, s, kvh)
+                const uint32_t bs = fdiv(y, pl.hkv);
+                const int kvh = static_cast<int>(y - bs * pl.hkv.d);
+                const uint32_t bq = fdiv(bs, pl.sink);
+                const int sidx = static_cast<int>(bs - bq * pl.sink.d);
+                const int b = static_cast<int>(bq);
                 const int64_t p0 = __ldg(a.p0 + b);
                 if (sidx < p0) {
                     if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + sidx) == sidx) {
@@ -180,23 +209,37 @@ int copy_grid(int64_t pieces) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t s) {
-    const int64_t pieces = static_cast<int64_t>(a.B) * a.n * a.H_kv * (2 * a.D / 8);
+    const int64_t rows = static_cast<int64_t>(a.B) * a.n * a.H_kv;
+    const int64_t pieces = rows * (2 * a.D / 8);
     if (pieces == 0) return cudaSuccess;
+    if (rows >= (int64_t{1} << 31) || a.n_slots - a.n_sink < 1) return cudaErrorInvalidValue;
+    CopyPlan pl{};
+    pl.hkv = fast_div(static_cast<uint32_t>(a.H_kv));
+    pl.n = fast_div(static_cast<uint32_t>(a.n));
+    pl.ring = fast_div(static_cast<uint32_t>(a.n_slots - a.n_sink));
+    pl.sink = fast_div(1);
     switch (a.D) {
-        case 64: append_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
-        case 128: append_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
-        case 256: append_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 64: append_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
+        case 128: append_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
+        case 256: append_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s) {
-    const int64_t pieces = static_cast<int64_t>(a.B) * (a.W - 1 + a.C + a.n_sink) * a.H_kv * (2 * a.D / 8);
+    const int64_t rows = static_cast<int64_t>(a.B) * (a.W - 1 + a.C + a.n_sink) * a.H_kv;
+    const int64_t pieces = rows * (2 * a.D / 8);
+    if (rows >= (int64_t{1} << 31) || a.n_slots - a.n_sink < 1) return cudaErrorInvalidValue;
+    CopyPlan pl{};
+    pl.hkv = fast_div(static_cast<uint32_t>(a.H_kv));
+    pl.n = fast_div(static_cast<uint32_t>(a.W - 1 + a.C));
+    pl.ring = fast_div(static_cast<uint32_t>(a.n_slots - a.n_sink));
+    pl.sink = fast_div(static_cast<uint32_t>(a.n_sink > 0 ? a.n_sink : 1));
     switch (a.D) {
-        case 64: gather_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
-        case 128: gather_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
-        case 256: gather_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a); break;
+        case 64: gather_kernel<64><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
+        case 128: gather_kernel<128><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
+        case 256: gather_kernel<256><<<copy_grid(pieces), kThreads, 0, s>>>(a, pl); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
