@@ -433,27 +433,45 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                     ok = false;
                     break;
                 }
-                for (int idx = w * 32 + lane; idx < rows * D; idx += 128) {
-                    const int r = idx / D, d = idx % D;
+                // eight threads per row: the row's split weights once, then float4 columns
+                // interleaved so each 8-thread phase reads 128 contiguous bytes
+                {
+                    const int t = w * 32 + lane;
+                    const int r = t >> 3, part = t & 7;
                     const int qs = qb * a.q_per_cta + r / group;
-                    if (qs >= a.NQ) continue;
-                    if (a.q_tok && (a.q_tok[qs] < 0 || a.q_tok[qs] >= a.tok_limit)) continue;
-                    const int h = kvh * group + r % group;
-                    float mw = -INFINITY;
+                    bool live = r < rows && qs < a.NQ;
+                    if (live && a.q_tok && (a.q_tok[qs] < 0 || a.q_tok[qs] >= a.tok_limit)) live = false;
+                    if (live) {
+                        const int h = kvh * group + r % group;
+                        float mw = -INFINITY;
 #pragma unroll
-                    for (int ww = 0; ww < 4; ++ww) mw = fmaxf(mw, red_m[ww * kSplitRows + r]);
-                    float s = 0.f, L = 0.f;
+                        for (int ww = 0; ww < 4; ++ww) mw = fmaxf(mw, red_m[ww * kSplitRows + r]);
+                        float f[4], L = 0.f;
 #pragma unroll
-                    for (int ww = 0; ww < 4; ++ww) {
-                        const float f = mw == -INFINITY ? 0.f : ex2(red_m[ww * kSplitRows + r] - mw);
-                        s += cbuf[(ww * kSplitRows + r) * C::CROW + d] * f;
-                        L += red_l[ww * kSplitRows + r] * f;
-                    }
-                    const int64_t row = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits + split;
-                    a.ws_acc[row * D + d] = s;
-                    if (d == 0) {
-                        a.ws_ml[row * 2 + 0] = mw;
-                        a.ws_ml[row * 2 + 1] = L;
+                        for (int ww = 0; ww < 4; ++ww) {
+                            f[ww] = mw == -INFINITY ? 0.f : ex2(red_m[ww * kSplitRows + r] - mw);
+                            L += red_l[ww * kSplitRows + r] * f[ww];
+                        }
+                        const int64_t row = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits + split;
+#pragma unroll
+                        for (int k4 = 0; k4 < D / 32; ++k4) {
+                            const int col = k4 * 32 + part * 4;
+                            float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int ww = 0; ww < 4; ++ww) {
+                                const float4 c4 =
+                                    *reinterpret_cast<const float4 *>(cbuf + (ww * kSplitRows + r) * C::CROW + col);
+                                acc4.x += c4.x * f[ww];
+                                acc4.y += c4.y * f[ww];
+                                acc4.z += c4.z * f[ww];
+                                acc4.w += c4.w * f[ww];
+                            }
+                            *reinterpret_cast<float4 *>(a.ws_acc + row * D + col) = acc4;
+                        }
+                        if (part == 0) {
+                            a.ws_ml[row * 2 + 0] = mw;
+                            a.ws_ml[row * 2 + 1] = L;
+                        }
                     }
                 }
                 __syncwarp();
