@@ -53,6 +53,7 @@ __device__ unsigned int g_band_err = 0;
 
 constexpr int BM = 128;              // query rows per tile (TMEM lanes)
 constexpr int kNarrow = 32;          // width of a narrow global-column tile
+constexpr int kShortTiles = 8;       // key tiles per unit at most for the short-band kernel
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 template <int D>
@@ -164,7 +165,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool kGlob>  // kGlob: the launch has global positions (global-column tiles)
+// kGlob: the launch has global positions (global-column tiles).  kShort: the band spans at
+// most kShortTiles key tiles per unit, so most tiles are band edges (or, with two query
+// tiles, beyond one tile's band): their masks take the cheaper forms below.
+template <int D, bool kGlob, bool kShort>
 __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     band_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const BandKernelArgs a) {
@@ -582,6 +586,20 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         continue;
                     }
                 }
+                if (kGlob && kShort && j < w.n_band) {
+                    // a band tile that none of this warp's rows reaches (the other query tile's
+                    // part of the unit's key range): P = 0 for these rows, nothing else changes
+                    const int k0 = w.kv_lo + j * BN;
+                    if (__all_sync(0xffffffffu, hi_abs < k0 || lo_abs > k0 + BN - 1 || hi_abs < lo_abs)) {
+#pragma unroll
+                        for (int hlf = 0; hlf < BN / 64; ++hlf) tmem_fill32(s_addr + hlf * 32, 0u);
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_pf(slot));
+                        continue;
+                    }
+                }
                 float x[BN];
                 {
                     uint32_t raw[BN / 32][32];
@@ -606,9 +624,19 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         const int hi = min(max(hi_abs - k0 + 1, 0), BN);
                         const int len = max(hi - lo, 0);
                         count += len;
+                        // short bands: one compare per column where the warp's rows are cut on
+                        // one side only
+                        if (kShort && __all_sync(0xffffffffu, hi == BN)) {
 #pragma unroll
-                        for (int c = 0; c < BN; ++c)
-                            x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
+                            for (int c = 0; c < BN; ++c) x[c] = c >= lo ? x[c] : -INFINITY;
+                        } else if (kShort && __all_sync(0xffffffffu, lo == 0)) {
+#pragma unroll
+                            for (int c = 0; c < BN; ++c) x[c] = c < hi ? x[c] : -INFINITY;
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < BN; ++c)
+                                x[c] = static_cast<unsigned>(c - lo) < static_cast<unsigned>(len) ? x[c] : -INFINITY;
+                        }
                     }
                     if (kGlob && a.sep) {
                         // with separate global projections a global key is scored (with
@@ -870,17 +898,21 @@ int band_sm_count() {
 template <int D>
 cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     using C = BandCfg<D>;
-    // launches without global positions take the kernel built without their code paths
+    // launches without global positions take the kernel built without their code paths;
+    // bands of at most kShortTiles key tiles per unit the one built for short bands
     const bool glob = x.n_global > 0;
-    auto kernel = glob ? band_fwd_kernel<D, true> : band_fwd_kernel<D, false>;
-    static bool configured[2] = {false, false};
-    if (!configured[glob]) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        configured[glob] = true;
-    }
     const int G = x.H_q / x.H_kv;
     const int TQ = BM / G;
+    const bool shrt = x.wl >= 0 && x.wr >= 0 &&
+                      (static_cast<long long>(C::NQT) * TQ - 1 + x.wl + x.wr) / C::BN + 2 <= kShortTiles;
+    auto kernel = glob ? (shrt ? band_fwd_kernel<D, true, true> : band_fwd_kernel<D, true, false>)
+                       : (shrt ? band_fwd_kernel<D, false, true> : band_fwd_kernel<D, false, false>);
+    static bool configured[2][2] = {{false, false}, {false, false}};
+    if (!configured[glob][shrt]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[glob][shrt] = true;
+    }
     CUtensorMap mq, mk, mv;
     const int Tk = x.Tk > 0 ? x.Tk : x.T;
     if (!make_map(&mq, x.q, D, x.H_q, x.T, x.B, x.q_st, G, TQ) ||

@@ -57,6 +57,10 @@ SMALL = [
     (2, 700, 8, 8, 64, 256, 256, [0, 350]),
     (1, 600, 4, 2, 256, 31, 0, [17]),
     (1, 389, 8, 4, 256, 129, 70, None),
+    # bands of more than eight key tiles per unit with global positions (the long-band
+    # kernel; the short ones above take the short-band kernel)
+    (1, 1500, 4, 2, 128, 1000, 0, [0, 3, 1499]),
+    (1, 1200, 8, 8, 64, 600, 600, [0, 600, 1199]),
 ]
 
 

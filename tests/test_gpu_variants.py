@@ -41,6 +41,7 @@ SINKS = [
     (1, 100, 4, 1, 128, 150, 0, [0, 1, 2, 3]),          # sinks inside every band
     (1, 700, 4, 2, 128, 100, 0, list(range(150))),      # two global-column tiles
     (1, 400, 2, 1, 64, 20, 3, [5, 77, 300]),            # sinks that are not the first tokens
+    (1, 1500, 4, 2, 128, 1000, 0, [0, 1, 2, 3]),        # long band (the long-band kernel)
 ]
 
 
