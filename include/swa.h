@@ -215,7 +215,8 @@ typedef struct swa_cache_params {
  * p0: device int32 [B], each >= 0 (a negative entry skips that sequence and is
  * reported by swa_check_device_error as SWA_ERR_INVALID_ARG).
  * Requirements: d_h in {64, 128, 256}; 0 <= n_sink < n_slots; pointers 16-byte
- * aligned (slot_pos, p0: 4-byte).  n_new = 0 is a no-op.
+ * aligned (slot_pos, p0: 4-byte); B * n_new * H_kv < 2^31 rows, else
+ * SWA_ERR_UNSUPPORTED.  n_new = 0 is a no-op.
  */
 SWA_API swa_status swa_cache_append(const swa_cache_params *c, const void *k_new, const void *v_new, int32_t n_new,
                             const int32_t *p0, swa_stream_t stream);
@@ -247,8 +248,8 @@ SWA_API swa_status swa_decode_append(const swa_decode_params *p, const void *k_n
  * positions) -- the tokens appended before the chunk; a slot found holding another
  * position is reported by swa_check_device_error as SWA_ERR_INVALID_ARG.
  * Requirements: the cache's B, H_kv, d_h match; window >= 1; H_q / H_kv <= 16; with
- * sinks, n_sink <= 128 and a ring of at least window - 1 slots (n_slots - n_sink), else
- * SWA_ERR_UNSUPPORTED.  Workspace: swa_prefill_chunk_workspace_size bytes, 256-byte
+ * sinks, n_sink <= 128 and a ring of at least window - 1 slots (n_slots - n_sink);
+ * B * (window - 1 + C + n_sink) * H_kv < 2^31 gathered rows; else SWA_ERR_UNSUPPORTED.  Workspace: swa_prefill_chunk_workspace_size bytes, 256-byte
  * aligned (the chunk's key/value rows and the window history gathered in position
  * order, and the sinks' rows).
  */

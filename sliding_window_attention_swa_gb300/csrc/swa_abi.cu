@@ -102,6 +102,10 @@ swa_status chunk_check(const swa_chunk_params *p, const swa_cache_params *c) {
     // a sink cache's ring must cover the window (its history is then contiguous)
     if (c->n_sink > 0 && c->n_slots - c->n_sink < p->window - 1) return SWA_ERR_UNSUPPORTED;
     if (c->n_sink > 128) return SWA_ERR_UNSUPPORTED;
+    // the gather's index arithmetic is 32-bit
+    if (static_cast<int64_t>(p->B) * (static_cast<int64_t>(p->window) - 1 + p->C + c->n_sink) * p->H_kv >=
+        (int64_t{1} << 31))
+        return SWA_ERR_UNSUPPORTED;
     if (!head_dim_ok(p->d_h)) return SWA_ERR_UNSUPPORTED;
     if (p->H_q / p->H_kv > swa::kSplitRows) return SWA_ERR_UNSUPPORTED;
     if (!scale_ok(p->scale)) return SWA_ERR_UNSUPPORTED;
@@ -458,6 +462,8 @@ swa_status swa_cache_append(const swa_cache_params *c, const void *k_new, const 
     if (n_new < 0 || (n_new > 0 && (!k_new || !v_new || !p0))) return SWA_ERR_INVALID_ARG;
     if (n_new == 0) return SWA_OK;
     if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(p0) & 3u)) return SWA_ERR_UNSUPPORTED;
+    // the append kernel's index arithmetic is 32-bit
+    if (static_cast<int64_t>(c->B) * n_new * c->H_kv >= (int64_t{1} << 31)) return SWA_ERR_UNSUPPORTED;
     if (failed(swa::launch_append(append_args(c, k_new, v_new, n_new, p0), reinterpret_cast<cudaStream_t>(stream))))
         return SWA_ERR_CUDA;
     return SWA_OK;

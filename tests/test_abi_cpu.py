@@ -181,6 +181,8 @@ def test_cache_append_arguments(lib):
     assert lib.swa_cache_append(ctypes.byref(c), None, 0x20000, 4, 0x30000, None) == 1
     assert lib.swa_cache_append(ctypes.byref(c), 0x20000, 0x20000, -1, 0x30000, None) == 1
     assert lib.swa_cache_append(ctypes.byref(c), 0x20008, 0x20000, 4, 0x30000, None) == 2
+    c.B, c.H_kv = 65536, 16
+    assert lib.swa_cache_append(ctypes.byref(c), 0x20000, 0x20000, 2048, 0x30000, None) == 2  # 2^31 rows
 
 
 def test_decode_append_rejects(lib):
@@ -201,6 +203,7 @@ def test_decode_append_rejects(lib):
     (lambda p, c: setattr(c, "n_sink", 4), 2),      # a sink cache whose ring (252) is shorter than window-1 (255)
     (lambda p, c: (setattr(c, "n_sink", 200), setattr(c, "n_slots", 600)), 2),  # more than 128 sinks
     (lambda p, c: setattr(p, "q", 0x10004), 2),
+    (lambda p, c: (setattr(p, "B", 4096), setattr(c, "B", 4096), setattr(p, "C", 1 << 18)), 2),  # >= 2^31 rows
 ])
 def test_prefill_chunk_rejects(lib, mutate, status):
     p, c = _valid_chunk(), _valid_cache()
