@@ -504,11 +504,22 @@ class OracleSampler:
         return self.oracle.num_threads()
 
 
+def kernel_code_digest(path: str) -> str:
+    """sha256 of a CUDA source with its comments and whitespace removed: a comment-only
+    edit leaves it unchanged, any change to the code changes it."""
+    import hashlib
+    import re
+
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()
+
+
 def band_traffic_per_launch():
     """DRAM bytes (read + write) of one band-kernel launch on the Mistral workload, from
-    the committed ncu summary -- only if it was captured from the current kernel source."""
-    import hashlib
-
+    the committed ncu summary -- only if it was captured from the current kernel code."""
     path = os.path.join(ROOT, "profiles", "band_fwd_mistral_traffic.txt")
     src = os.path.join(ROOT, "sliding_window_attention_swa_gb300", "csrc", "swa_band.cu")
     try:
@@ -518,9 +529,7 @@ def band_traffic_per_launch():
                 if line.strip() and not line.startswith("#"):
                     k, v = line.split(None, 1)
                     fields[k] = v.strip()
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        if fields.get("kernel_source_sha256") != digest:
+        if fields.get("kernel_code_sha256") != kernel_code_digest(src):
             return None
         return int(fields["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):

@@ -23,8 +23,8 @@
 //   warp 1        TMEM owner and MMA issuer (one thread):
 //                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
-//   warp 2        Q loader: a unit's query tiles as soon as the previous unit's S
-//                 MMAs have finished reading that shared memory.
+//   warp 2        Q loader: a unit's query tiles once every MMA of the previous unit
+//                 has completed (its S MMAs were the last to read that shared memory).
 //   softmax WGs   NQT warpgroups; one row per thread (TMEM lane).  Scores are masked
 //                 only on band-edge and global tiles; the running max is kept in the
 //                 log2 domain; P = 2^(x - m) is written back as bf16 over the S
@@ -35,6 +35,10 @@
 // NQT = 2 (head dim <= 128): two query tiles ping-pong -- while one warpgroup turns
 // S_A into P_A the tensor cores run S_B and P_B V -- with TMEM S_A | S_B | O_A | O_B.
 // NQT = 1 (head dim 256): one query tile, S double-buffered, TMEM S0 | S1 | O.
+// Builds per head dim: with and without global-position code (kGlob), and for long and
+// short bands (kShort: at most kShortTiles key tiles per unit, where most tiles are band
+// edges or lie beyond one query tile's band).  At most kNarrow global positions take one
+// kNarrow-key global-column tile (S with N = kNarrow, P V with K = kNarrow).
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and MMAs, frees TMEM and returns.
 #include <cfloat>
