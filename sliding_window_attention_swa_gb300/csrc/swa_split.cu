@@ -10,7 +10,7 @@
 //
 // Persistent kernel, two CTAs per SM for head dim <= 128 (one for 256), five warps:
 //   warp 0     producer.  Walks this CTA's work items (batch, kv head, query block,
-//              1024-slot split) in a static round-robin order.  For each item it
+//              split of at most 1024 slots) in a static round-robin order.  For each item it
 //              reads the slot positions, builds one 64-bit validity mask per
 //              64-slot chunk, writes the split's valid count, and streams the K and
 //              V of every chunk that has a valid slot into a ring of NST stages
@@ -22,7 +22,10 @@
 //              and write the split's partial.  Value rows of invalid slots are
 //              zeroed before P V, so whatever an unwritten slot holds (even NaN)
 //              never reaches the result.
-// The merge kernel combines the splits of a row (FlashAttention-style rescaling).
+// The merge kernel combines the splits of a row (log-sum-exp rescaling).  It is launched
+// as a programmatic dependent of the split pass, and the global-row split pass as one
+// of the band kernel before it (it reads only q/k/v); griddepcontrol.wait orders each
+// consumer after the grid whose results it reads.
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and returns.
 #include <cfloat>
