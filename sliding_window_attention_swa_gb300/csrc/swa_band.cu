@@ -82,7 +82,7 @@ struct BandCfg {
     static constexpr int NSLOT = (232448 - 2048 - OFF_RING) / TBYTES;
     static constexpr int OFF_BAR = OFF_RING + NSLOT * TBYTES;
     // q_full[2], q_empty[2], kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2],
-    // o_done[2], o_free[2], pv_done[2], drain
+    // o_done[2], o_free[2], two unused words, drain
     static constexpr int NBAR = 2 * NSLOT + 15;
     static constexpr int OFF_TMEMPTR = OFF_BAR + NBAR * 8;
     // global positions of a list of at most BN entries, staged once per CTA
@@ -196,7 +196,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     auto bar_pf = [&](int i) { return bars + 8u * (6 + 2 * NSLOT + i); };
     auto bar_od = [&](int i) { return bars + 8u * (8 + 2 * NSLOT + i); };
     auto bar_of = [&](int i) { return bars + 8u * (10 + 2 * NSLOT + i); };
-    auto bar_pv = [&](int i) { return bars + 8u * (12 + 2 * NSLOT + i); };
     const uint32_t bar_drain = bars + 8u * (14 + 2 * NSLOT);
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
     int *gpos = reinterpret_cast<int *>(sgen + C::OFF_GPOS);
@@ -215,7 +214,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             mbar_init(bar_pf(x), 4);
             mbar_init(bar_od(x), 1);
             mbar_init(bar_of(x), 4);
-            mbar_init(bar_pv(x), 1);
         }
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(bar_full(s), 1);
@@ -452,7 +450,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         }
                         ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0, narrow(j));
                         if (!ok) break;
-                        tc_commit(bar_pv(jg & 1));
                         tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 == n) tc_commit(bar_od(0));
                     }
@@ -541,9 +538,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         const float mu = need ? mt : m;
                         const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
                         if (__any_sync(0xffffffffu, need) && j > 0) {
-                            // O holds P V of tiles 0 .. j-1 of this unit and must be complete.
+                            // O holds P V of tiles 0 .. j-1 of this unit and must be complete:
+                            // the release of tile j-1's V slot (fill 2(j-1)+1) is committed
+                            // right after that P V
                             if constexpr (NQT == 1) {
-                                if (!warp_wait(bar_pv((jg - 1) & 1), ((jg - 1) >> 1) & 1, abort)) {
+                                if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), ((2 * (jg - 1) + 1) / NSLOT) & 1,
+                                               abort)) {
                                     ok = false;
                                     break;
                                 }
@@ -738,9 +738,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const float mu = need ? mt : m;
                 const float alpha = need ? ex2(m - mu) : 1.f;  // m = -inf gives 0
                 if (__any_sync(0xffffffffu, need) && j > 0) {
-                    // O holds P V of tiles 0 .. j-1 of this unit and must be complete.
+                    // O holds P V of tiles 0 .. j-1 of this unit and must be complete: the
+                    // release of tile j-1's V slot (fill 2(j-1)+1) is committed right after
+                    // that P V (no commit of its own on the issuing thread)
                     if constexpr (NQT == 1) {
-                        if (!warp_wait(bar_pv((jg - 1) & 1), ((jg - 1) >> 1) & 1, abort)) {
+                        if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), ((2 * (jg - 1) + 1) / NSLOT) & 1,
+                                       abort)) {
                             ok = false;
                             break;
                         }

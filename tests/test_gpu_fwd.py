@@ -155,3 +155,30 @@ def test_full_size_workloads(cfg):
     o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, rows=rows)
     b, h, t = rows[:, 0], rows[:, 1], rows[:, 2]
     assert_parity(o[b, h, t], lse[b, h, t], cnt[b, h, t], o_ref, lse_ref, cnt_ref, cfg.name)
+
+
+RAMP = [
+    # B, T, Hq, Hkv, d, wl, wr
+    (1, 700, 4, 2, 128, 699, 0),   # two query tiles per unit
+    (1, 700, 4, 2, 64, 300, 300),
+    (1, 500, 4, 2, 256, 499, 0),   # one query tile, S double-buffered
+]
+
+
+@pytest.mark.parametrize("case", RAMP, ids=[f"T{c[1]}-d{c[4]}-wl{c[5]}-wr{c[6]}" for c in RAMP])
+def test_growing_scores_rescale_o(case):
+    """Keys whose scores grow along the sequence, by far more than 2^8 per key tile, so
+    every row's running max keeps rising and O is rescaled in TMEM on every tile (the
+    lazy rescale path); checked against the oracle like any other case."""
+    B, T, Hq, Hkv, d, wl, wr = case
+    seed = 11 * T + d
+    q = I.bf16_bits_to_f32(I.normal_bf16(seed, (B, T, Hq, d))) * 0.5 + 0.5
+    k = I.bf16_bits_to_f32(I.normal_bf16(seed + 1, (B, T, Hkv, d))) * 0.5
+    ramp = (np.arange(T, dtype=np.float32) / 8.0)[None, :, None, None]
+    k = k + ramp * 0.25   # scale * q.k grows by ~sqrt(d) * 4 per 128 keys
+    v = I.normal_bf16(seed + 2, (B, T, Hkv, d))
+    qb, kb = I.f32_to_bf16_bits(q.astype(np.float32)), I.f32_to_bf16_bits(k.astype(np.float32))
+    scale = d ** -0.5
+    o, lse, cnt = _run(qb, kb, v, wl, wr, scale, None)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(qb, kb, v, wl, wr, scale, None)
+    assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, str(case))
