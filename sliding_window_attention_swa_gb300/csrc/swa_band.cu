@@ -197,6 +197,14 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     auto bar_od = [&](int i) { return bars + 8u * (8 + 2 * NSLOT + i); };
     auto bar_of = [&](int i) { return bars + 8u * (10 + 2 * NSLOT + i); };
     const uint32_t bar_drain = bars + 8u * (14 + 2 * NSLOT);
+    // NQT = 1: only value fills release their slot (a tile's S MMAs precede its P V, so the
+    // release of V_j also frees K_j's slot).  With an odd ring, a slot alternates key and
+    // value fills, so its barrier counts value fills only: the phase of value fill p.
+    static_assert(NQT == 2 || NSLOT % 2 == 1, "value-only slot releases need an odd ring");
+    auto vpar = [&](int p) -> uint32_t {
+        const int sl = p % NSLOT, i = p / NSLOT;
+        return static_cast<uint32_t>(((i - ((1 + sl) & 1)) / 2) & 1);
+    };
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
     int *gpos = reinterpret_cast<int *>(sgen + C::OFF_GPOS);
     // A list of at most BN positions is staged in shared memory for the global-column mask.
@@ -252,7 +260,15 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
             for (int i = 0; i < 2 * w.n_tiles; ++i) {
                 const int s = g % NSLOT;
-                if (g >= NSLOT) ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
+                if (g >= NSLOT) {
+                    if constexpr (NQT == 1) {
+                        // the slot's last fill, or (a key fill) the value fill of its tile
+                        const int prev = g - NSLOT, vp = (prev & 1) ? prev : prev + 1;
+                        ok = warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
+                    } else {
+                        ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
+                    }
+                }
                 if (!ok) break;
                 const int j = i >> 1;
                 const bool is_v = (i & 1) != 0;
@@ -436,7 +452,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     ok = mma_s(J & 1, 0, J, true, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(J & 1));
-                        tc_commit(bar_empty(kslot(J)));
                     }
 #pragma unroll 1
                     for (int j = 0; j < n && ok; ++j) {
@@ -446,7 +461,6 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             ok = mma_s((jg + 1) & 1, 0, jg + 1, true, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf((jg + 1) & 1));
-                            tc_commit(bar_empty(kslot(jg + 1)));
                         }
                         ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0, narrow(j));
                         if (!ok) break;
@@ -542,7 +556,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             // the release of tile j-1's V slot (fill 2(j-1)+1) is committed
                             // right after that P V
                             if constexpr (NQT == 1) {
-                                if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), ((2 * (jg - 1) + 1) / NSLOT) & 1,
+                                if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), vpar(2 * (jg - 1) + 1),
                                                abort)) {
                                     ok = false;
                                     break;
@@ -742,7 +756,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     // release of tile j-1's V slot (fill 2(j-1)+1) is committed right after
                     // that P V (no commit of its own on the issuing thread)
                     if constexpr (NQT == 1) {
-                        if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), ((2 * (jg - 1) + 1) / NSLOT) & 1,
+                        if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), vpar(2 * (jg - 1) + 1),
                                        abort)) {
                             ok = false;
                             break;
