@@ -205,6 +205,17 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         const int sl = p % NSLOT, i = p / NSLOT;
         return static_cast<uint32_t>(((i - ((1 + sl) & 1)) / 2) & 1);
     };
+    // NQT = 2: only key fills release their slot (V_j's last reader, P V_B(j), is issued
+    // before K_{j+1}'s, S_B(j+1)), so a value fill's slot is free once the next key fill's
+    // is.  The phase of key fill p on its slot's barrier: an odd ring alternates key and
+    // value fills per slot, an even one keeps them in slots of their own.
+    // (Not in the long-band build with global positions, where a unit's last value slot,
+    // held across the boundary until the next unit's first key is released, cost 1.8%.)
+    constexpr bool kKeyRel = NQT == 2 && !(kGlob && !kShort);
+    auto kpar = [&](int p) -> uint32_t {
+        const int sl = p % NSLOT, i = p / NSLOT;
+        return static_cast<uint32_t>((NSLOT % 2 == 1 ? (i - (sl & 1)) / 2 : i) & 1);
+    };
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEMPTR);
     int *gpos = reinterpret_cast<int *>(sgen + C::OFF_GPOS);
     // A list of at most BN positions is staged in shared memory for the global-column mask.
@@ -265,6 +276,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         // the slot's last fill, or (a key fill) the value fill of its tile
                         const int prev = g - NSLOT, vp = (prev & 1) ? prev : prev + 1;
                         ok = warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
+                    } else if constexpr (kKeyRel) {
+                        // the slot's last fill, or (a value fill) the key fill of the next tile
+                        const int prev = g - NSLOT, kp = (prev & 1) ? prev + 1 : prev;
+                        ok = warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
                     } else {
                         ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
                     }
@@ -438,7 +453,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         }
                         ok = mma_pv(1, 1, jg, jg & 1, false, j == 0, narrow(j));
                         if (!ok) break;
-                        tc_commit(bar_empty(vslot(jg)));
+                        if constexpr (!kKeyRel) tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 < n) {
                             ok = mma_s(1, 1, jg + 1, false, narrow(j + 1));
                             if (!ok) break;
