@@ -23,7 +23,9 @@
 //                 tiles and no global positions, V_j and K_{j+1} are copied together
 //                 and signal one barrier (that of K_{j+1}'s slot): the issuing thread
 //                 then waits once per key tile, before P_A V_j, and S_A(j+1) needs no
-//                 wait of its own.
+//                 wait of its own.  Ring slots are released by key fills only (a value
+//                 fill's last reader precedes the next key fill's); in those builds the
+//                 release is an arrive by softmax warpgroup B once it sees S_B(j) done.
 //   warp 1        TMEM owner and MMA issuer (one thread):
 //                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
@@ -221,6 +223,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     // slot barrier then completes only for key fills (and for the CTA's last value fill,
     // which has no key fill after it): the parity of owner fill q's completion.
     constexpr bool kPair = NQT == 2 && !kGlob;
+    // kSoftRel (the same builds): softmax warpgroup B, which waits for S_B(j) anyway,
+    // releases K_j's slot instead of a commit on the issuing thread
+    constexpr bool kSoftRel = kPair;
     auto fpar = [&](int q) -> uint32_t {
         const int sl = q % NSLOT, i = q / NSLOT;
         const int n = NSLOT % 2 == 1 ? (i - (sl & 1) + 1) / 2 : (sl % 2 == 0 ? i : 0);
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     if (ok) ok = mma_s(1, 1, J, false, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(1));
-                        tc_commit(bar_empty(kslot(J)));
+                        if constexpr (!kSoftRel) tc_commit(bar_empty(kslot(J)));
                     }
 #pragma unroll 1
                     for (int j = 0; j < n && ok; ++j) {
@@ -544,7 +549,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             ok = mma_s(1, 1, jg + 1, false, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf(1));
-                            tc_commit(bar_empty(kslot(jg + 1)));
+                            if constexpr (!kSoftRel) tc_commit(bar_empty(kslot(jg + 1)));
                         } else {
                             tc_commit(bar_od(1));
                         }
@@ -611,6 +616,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (!warp_wait(bar_sf(slot), parity, abort)) {
                     ok = false;
                     break;
+                }
+                if constexpr (kSoftRel) {
+                    // S_B(jg) was the last MMA issued before this commit: every reader of
+                    // K_jg (and of V_{jg-1}) is done, so the key fill's slot is released here
+                    // rather than by another commit on the issuing thread
+                    if (wg == 1 && quarter == 0 && lane == 0) mbar_arrive(bar_empty((2 * jg) % NSLOT));
                 }
                 tc_fence_after();
                 const uint32_t s_addr = tmem + lane_addr + C::tm_s(slot);
