@@ -23,7 +23,8 @@
 //                 tiles and no global positions, V_j and K_{j+1} are copied together
 //                 and signal one barrier (that of K_{j+1}'s slot): the issuing thread
 //                 then waits once per key tile, before P_A V_j, and S_A(j+1) needs no
-//                 wait of its own.  Ring slots are released by key fills only (a value
+//                 wait of its own.  With one query tile (no global positions) the same
+//                 pairing lets the wait before S(j+1) cover V_j's P V.  Ring slots are released by key fills only (a value
 //                 fill's last reader precedes the next key fill's); in those builds the
 //                 release is an arrive by softmax warpgroup B once it sees S_B(j) done.
 //   warp 1        TMEM owner and MMA issuer (one thread):
@@ -218,14 +219,15 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     // (Not in the long-band build with global positions, where a unit's last value slot,
     // held across the boundary until the next unit's first key is released, cost 1.8%.)
     constexpr bool kKeyRel = NQT == 2 && !(kGlob && !kShort);
-    // kPair (two query tiles, no global positions): V_j and K_{j+1} are copied together
-    // on K_{j+1}'s slot barrier, so one wait before P V_A(j) covers S_A(j+1) as well.  A
-    // slot barrier then completes only for key fills (and for the CTA's last value fill,
-    // which has no key fill after it): the parity of owner fill q's completion.
-    constexpr bool kPair = NQT == 2 && !kGlob;
-    // kSoftRel (the same builds): softmax warpgroup B, which waits for S_B(j) anyway,
+    // kPair (no global positions): V_j and K_{j+1} are copied together on K_{j+1}'s slot
+    // barrier, so one wait covers both: before P V_A(j) with two query tiles (S_A(j+1)
+    // follows), before S(j+1) with one (P V(j) follows).  A slot barrier then completes
+    // only for key fills (and for the CTA's last value fill, which has no key fill after
+    // it): fpar(q) is the parity of owner fill q's completion.
+    constexpr bool kPair = !kGlob;
+    // kSoftRel (those builds with two query tiles): softmax warpgroup B, which waits for S_B(j) anyway,
     // releases K_j's slot instead of a commit on the issuing thread
-    constexpr bool kSoftRel = kPair;
+    constexpr bool kSoftRel = kPair && NQT == 2;
     auto fpar = [&](int q) -> uint32_t {
         const int sl = q % NSLOT, i = q / NSLOT;
         const int n = NSLOT % 2 == 1 ? (i - (sl & 1) + 1) / 2 : (sl % 2 == 0 ? i : 0);
@@ -295,8 +297,14 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             // its last occupant (a value fill), has been released
             auto slot_free = [&](int p) -> bool {
                 if (p < NSLOT) return true;
-                const int prev = p - NSLOT, kp = (prev & 1) ? prev + 1 : prev;
-                return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
+                const int prev = p - NSLOT;
+                if constexpr (NQT == 1) {
+                    const int vp = (prev & 1) ? prev : prev + 1;  // value fills release
+                    return warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
+                } else {
+                    const int kp = (prev & 1) ? prev + 1 : prev;  // key fills release
+                    return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
+                }
             };
             auto copy = [&](const Unit &w, int j, bool is_v, int slot, uint32_t bar) {
                 const int k0 = w.kv_lo + j * BN;
@@ -467,7 +475,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
             auto mma_s = [&](int slot, int qt, int jg, bool wait_k, bool narrow = false) -> bool {
                 const int fi = 2 * jg, s = fi % NSLOT;
-                if (wait_k && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
+                // paired fills: a key fill owns its barrier (with V_{jg-1} on it); with two
+                // query tiles only the CTA's first key tile is waited for here (phase 0)
+                const uint32_t kpty = kPair && NQT == 1 ? fpar(fi) : static_cast<uint32_t>((fi / NSLOT) & 1);
+                if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
 #pragma unroll
@@ -568,7 +579,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             if (!ok) break;
                             tc_commit(bar_sf((jg + 1) & 1));
                         }
-                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, true, j == 0, narrow(j));
+                        // paired fills: V_jg came with K_{jg+1}, waited for by S(jg+1) just above
+                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, !kPair || j + 1 == n, j == 0, narrow(j));
                         if (!ok) break;
                         tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 == n) tc_commit(bar_od(0));
