@@ -61,6 +61,13 @@ SMALL = [
     # kernel; the short ones above take the short-band kernel)
     (1, 1500, 4, 2, 128, 1000, 0, [0, 3, 1499]),
     (1, 1200, 8, 8, 64, 600, 600, [0, 600, 1199]),
+    # more units than persistent CTAs, each of one to five key tiles: the K/V ring runs
+    # across unit boundaries (a unit's last V_j shares a barrier with the next unit's K_0)
+    (8, 1024, 8, 2, 128, 63, 0, None),     # 256 units of 1-2 tiles
+    (8, 1024, 8, 2, 128, 0, 0, None),      # 256 units of exactly one tile; o_t = v_t
+    (2, 2048, 8, 8, 256, 99, 0, None),     # one query tile per unit: 256 units of 4-5 tiles
+    (2, 2048, 8, 8, 256, 0, 0, None),      # 256 units of two 64-key tiles; o_t = v_t
+    (6, 1024, 8, 4, 64, 40, 40, None),     # 192 short-band units
 ]
 
 
