@@ -54,6 +54,8 @@
  *   read (and cleared) by swa_check_device_error().
  * - Thread safety: calls may be made from several host threads on different
  *   streams; workspaces must not be shared between calls that overlap in time.
+ *   One-time per-device setup (kernel attributes, SM counts) is cached in atomics,
+ *   so one process may also drive several devices (the current device is used).
  */
 #ifndef SWA_H
 #define SWA_H

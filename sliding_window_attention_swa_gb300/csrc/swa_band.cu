@@ -48,6 +48,7 @@
 // kNarrow-key global-column tile (S with N = kNarrow, P V with K = kNarrow).
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and MMAs, frees TMEM and returns.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -1029,15 +1030,15 @@ bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int B, cons
 }
 
 int band_sm_count() {
-    static int n[64] = {};
+    static std::atomic<int> n[64];  // per device; 0 = not looked up yet
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) {
-        int v = 0;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-        n[dev] = v;
+        n[dev].store(v, std::memory_order_relaxed);
     }
-    return n[dev];
+    return v;
 }
 
 template <int D>
@@ -1052,11 +1053,14 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
                       (static_cast<long long>(C::NQT) * TQ - 1 + x.wl + x.wr) / C::BN + 2 <= kShortTiles;
     auto kernel = glob ? (shrt ? band_fwd_kernel<D, true, true> : band_fwd_kernel<D, true, false>)
                        : (shrt ? band_fwd_kernel<D, false, true> : band_fwd_kernel<D, false, false>);
-    static bool configured[2][2] = {{false, false}, {false, false}};
-    if (!configured[glob][shrt]) {
+    // the dynamic shared-memory limit is a per-device function attribute: set once per device
+    static std::atomic<bool> configured[64][2][2];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) dev = -1;
+    if (dev < 0 || !configured[dev][glob][shrt].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        configured[glob][shrt] = true;
+        if (dev >= 0) configured[dev][glob][shrt].store(true, std::memory_order_release);
     }
     CUtensorMap mq, mk, mv;
     const int Tk = x.Tk > 0 ? x.Tk : x.T;

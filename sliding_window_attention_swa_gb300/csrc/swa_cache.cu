@@ -7,6 +7,7 @@
 // n_sink + (p - n_sink) mod (n_slots - n_sink).
 //
 // Both kernels are pure copies, bound by HBM, moving 16-byte pieces.
+#include <atomic>
 #include <climits>
 
 #include "swa_internal.h"
@@ -190,14 +191,15 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a, co
 }
 
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess)
-            n = 148;
+    static std::atomic<int> n[64];  // per device; 0 = not looked up yet
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev].store(v, std::memory_order_relaxed);
     }
-    return n;
+    return v;
 }
 
 int copy_grid(int64_t pieces) {

@@ -28,6 +28,7 @@
 // consumer after the grid whose results it reads.
 // Every wait is bounded; on expiry the CTA records an error word, drains its
 // copies and returns.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -561,25 +562,28 @@ bool slot_map(CUtensorMap *m, const void *base, int D, int n_slots, int H, int B
 }
 
 int sm_count() {
-    static int n[64] = {};
+    static std::atomic<int> n[64];  // per device; 0 = not looked up yet
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!n[dev]) {
-        int v = 0;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-        n[dev] = v;
+        n[dev].store(v, std::memory_order_relaxed);
     }
-    return n[dev];
+    return v;
 }
 
 template <int D>
 cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
     using C = StreamCfg<D>;
-    static bool configured = false;
-    if (!configured) {
+    // the dynamic shared-memory limit is a per-device function attribute: set once per device
+    static std::atomic<bool> configured[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) dev = -1;
+    if (dev < 0 || !configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(stream_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        configured = true;
+        if (dev >= 0) configured[dev].store(true, std::memory_order_release);
     }
     if (a.slots_per_split <= 0 || a.slots_per_split > kSlotsPerSplit || a.slots_per_split % CH != 0 ||
         static_cast<int64_t>(a.slots_per_split) * a.n_splits < a.n_slots)
