@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity import assert_parity, i32_dev, to_dev, to_host_f64
+from parity import assert_parity, compare_every_row, i32_dev, to_dev, to_host_f64
 from sliding_window_attention_swa_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -152,16 +152,31 @@ def _sample_rows(cfg, rng, n_random=96):
 
 @pytest.mark.parametrize("cfg", [I.MISTRAL, I.GEMMA_LOCAL, I.LONGFORMER], ids=lambda c: c.name)
 def test_full_size_workloads(cfg):
-    """Full-size prefill / encoder workloads: every row's count, sampled rows' O and lse."""
+    """Full-size prefill / encoder workloads: every row's count against the closed form,
+    then sampled edge rows (a fast first check), then every row's O and lse against the
+    oracle, a few heads at a time."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
     q, k, v = I.prefill_inputs(cfg)
     G = list(cfg.globals_) or None
-    o, lse, cnt = _run(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G)
-    want = _closed_form_counts(cfg.T, cfg.window_left, cfg.window_right, G)
+    wl, wr = cfg.window_left, cfg.window_right
+    od, lsed, cntd = swa.swa_fwd(to_dev(q), to_dev(k), to_dev(v), wl, wr, cfg.scale,
+                                 None if G is None else i32_dev(G), want_counts=True)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o = od.cpu()  # [B, T, Hq, d] bf16
+    del od
+    lse, cnt = lsed.cpu().numpy().astype(np.float64), cntd.cpu().numpy()
+    want = _closed_form_counts(cfg.T, wl, wr, G)
     assert (cnt == want[None, None, :]).all(), "attended-key counts differ from the closed form"
     rows = _sample_rows(cfg, np.random.default_rng(cfg.seed))
-    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, rows=rows)
+    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, wl, wr, cfg.scale, G, rows=rows)
     b, h, t = rows[:, 0], rows[:, 1], rows[:, 2]
-    assert_parity(o[b, h, t], lse[b, h, t], cnt[b, h, t], o_ref, lse_ref, cnt_ref, cfg.name)
+    og = o[torch.from_numpy(b), torch.from_numpy(t), torch.from_numpy(h)].to(torch.float64).numpy()
+    assert_parity(og, lse[b, h, t], cnt[b, h, t], o_ref, lse_ref, cnt_ref, cfg.name + " (sampled rows)")
+    compare_every_row(cfg.name, o, lse, cnt, lambda r: oracle.fwd(q, k, v, wl, wr, cfg.scale, G, rows=r),
+                      cfg.B, cfg.Hq, cfg.T)
 
 
 RAMP = [

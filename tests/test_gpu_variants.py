@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity import assert_parity, i32_dev, to_dev, to_host_f64
+from parity import assert_parity, compare_every_row, i32_dev, to_dev, to_host_f64
 from sliding_window_attention_swa_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -29,6 +29,21 @@ def _run(q, k, v, wl, wr, scale, G=None, **kw):
     torch.cuda.synchronize()
     swa.swa_check_device_error()
     return to_host_f64(o).transpose(0, 2, 1, 3), lse.cpu().numpy().astype(np.float64), cnt.cpu().numpy()
+
+
+def _run_full(q, k, v, wl, wr, scale, G=None, **kw):
+    """As _run, for full-size outputs: O stays bf16 [B, T, Hq, d] on the host."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    for name in ("q_g", "k_g", "v_g"):
+        if kw.get(name) is not None:
+            kw[name] = to_dev(kw[name])
+    g = None if G is None else i32_dev(G)
+    o, lse, cnt = swa.swa_fwd(to_dev(q), to_dev(k), to_dev(v), wl, wr, scale, g, want_counts=True, **kw)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    return o.cpu(), lse.cpu().numpy().astype(np.float64), cnt.cpu().numpy()
 
 
 # ----------------------------------------------------------------------------- sinks
@@ -57,22 +72,19 @@ def test_sinks(case):
 
 def test_sinks_full_size_mistral():
     """Mistral-shape causal prefill with four pinned sinks: every row's count against
-    the closed form min(t+1, W) + max(0, min(4, t-W+1)), sampled rows' O and lse."""
+    the closed form min(t+1, W) + max(0, min(4, t-W+1)), every row's O and lse against
+    the oracle."""
     cfg = I.MISTRAL
     q, k, v = I.prefill_inputs(cfg)
     G = [0, 1, 2, 3]
     W = cfg.window_left + 1
-    o, lse, cnt = _run(q, k, v, cfg.window_left, 0, cfg.scale, G, global_mode=oracle.GLOBAL_SINK)
+    o, lse, cnt = _run_full(q, k, v, cfg.window_left, 0, cfg.scale, G, global_mode=oracle.GLOBAL_SINK)
     t = np.arange(cfg.T)
     want = np.minimum(t + 1, W) + np.maximum(0, np.minimum(4, t - W + 1))
     assert (cnt == want[None, None, :]).all()
-    rng = np.random.default_rng(5)
-    ts = sorted({0, 3, 4, W - 1, W, W + 1, W + 3, W + 4, cfg.T - 1} | set(int(x) for x in rng.integers(0, cfg.T, 40)))
-    rows = np.array([(0, int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
-    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, 0, cfg.scale, G, rows=rows,
-                                         gmode=oracle.GLOBAL_SINK)
-    b, h, tt = rows[:, 0], rows[:, 1], rows[:, 2]
-    assert_parity(o[b, h, tt], lse[b, h, tt], cnt[b, h, tt], o_ref, lse_ref, cnt_ref, "mistral+sinks")
+    compare_every_row("mistral+4 sinks", o, lse, cnt,
+                      lambda r: oracle.fwd(q, k, v, cfg.window_left, 0, cfg.scale, G, rows=r,
+                                           gmode=oracle.GLOBAL_SINK), cfg.B, cfg.Hq, cfg.T)
 
 
 # ----------------------------------------------------------------------------- narrow global tile
@@ -123,21 +135,18 @@ def test_separate_global_projections(case):
 
 
 def test_separate_projections_full_size_longformer():
+    """Longformer-shape encoder with separate global projections: every row's O, lse
+    and count against the oracle."""
     cfg = I.LONGFORMER
     q, k, v = I.prefill_inputs(cfg)
     qg = I.normal_bf16(cfg.seed * 16 + 8, q.shape)
     kg = I.normal_bf16(cfg.seed * 16 + 9, k.shape)
     vg = I.normal_bf16(cfg.seed * 16 + 10, v.shape)
     G = list(cfg.globals_)
-    o, lse, cnt = _run(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, q_g=qg, k_g=kg, v_g=vg)
-    rng = np.random.default_rng(9)
-    ts = sorted({0, 1, 255, 256, 257, 2047, 2048, 2049, 1792, 2304, cfg.T - 1} |
-                set(int(x) for x in rng.integers(0, cfg.T, 60)))
-    rows = np.array([(int(rng.integers(0, cfg.B)), int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
-    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, rows=rows,
-                                         qg=qg, kg=kg, vg=vg)
-    b, h, t = rows[:, 0], rows[:, 1], rows[:, 2]
-    assert_parity(o[b, h, t], lse[b, h, t], cnt[b, h, t], o_ref, lse_ref, cnt_ref, "longformer+Qg/Kg/Vg")
+    o, lse, cnt = _run_full(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, q_g=qg, k_g=kg, v_g=vg)
+    compare_every_row("longformer+Qg/Kg/Vg", o, lse, cnt,
+                      lambda r: oracle.fwd(q, k, v, cfg.window_left, cfg.window_right, cfg.scale, G, rows=r,
+                                           qg=qg, kg=kg, vg=vg), cfg.B, cfg.Hq, cfg.T)
 
 
 # ----------------------------------------------------------------------------- dilation
@@ -163,23 +172,21 @@ def test_dilation(case):
 
 def test_dilation_full_size_longformer():
     """Longformer-shape encoder, heads 8-11 dilated by 2 (no globals): every row's
-    count against the residue-class closed form, sampled rows' O and lse."""
+    count against the residue-class closed form, every row's O and lse against the
+    oracle."""
     cfg = I.LONGFORMER
     q, k, v = I.prefill_inputs(cfg)
     dil = [1] * 8 + [2] * 4
     r = cfg.window_left
-    o, lse, cnt = _run(q, k, v, r, r, cfg.scale, dilation=dil)
+    o, lse, cnt = _run_full(q, k, v, r, r, cfg.scale, dilation=dil)
     t = np.arange(cfg.T)
     for h in range(cfg.Hq):
         d = dil[h]
         want = np.minimum(r, t // d) + np.minimum(r, (cfg.T - 1 - t) // d) + 1
         assert (cnt[:, h] == want[None, :]).all(), h
-    rng = np.random.default_rng(13)
-    ts = sorted({0, 1, 255, 256, 511, 512, 513, cfg.T - 2, cfg.T - 1} | set(int(x) for x in rng.integers(0, cfg.T, 60)))
-    rows = np.array([(int(rng.integers(0, cfg.B)), int(rng.integers(0, cfg.Hq)), x) for x in ts], dtype=np.int64)
-    o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, r, r, cfg.scale, rows=rows, dilation=dil)
-    b, h, tt = rows[:, 0], rows[:, 1], rows[:, 2]
-    assert_parity(o[b, h, tt], lse[b, h, tt], cnt[b, h, tt], o_ref, lse_ref, cnt_ref, "longformer dilated")
+    compare_every_row("longformer dilation mix", o, lse, cnt,
+                      lambda rows: oracle.fwd(q, k, v, r, r, cfg.scale, rows=rows, dilation=dil),
+                      cfg.B, cfg.Hq, cfg.T)
 
 
 # ----------------------------------------------------------------------------- decode window / sinks
