@@ -50,8 +50,11 @@
  *   synchronising.  Argument errors are detected on the host and returned before
  *   anything is launched.  SWA_ERR_CUDA reports a failed launch.
  * - Bounded waits: every wait inside a kernel has a time limit; on expiry the
- *   kernel records an error word in device memory and returns.  The word is
- *   read (and cleared) by swa_check_device_error().
+ *   kernel records an error word in device memory, drains its own copies and
+ *   tensor-core work, frees its tensor memory and returns, so the CUDA context stays
+ *   usable.  The words are read (and cleared) by swa_check_device_error() or
+ *   swa_read_device_errors().  They are per device, shared by every stream and
+ *   every call on it.
  * - Thread safety: calls may be made from several host threads on different
  *   streams; workspaces must not be shared between calls that overlap in time.
  *   One-time per-device setup (kernel attributes, SM counts) is cached in atomics,
@@ -97,7 +100,11 @@ typedef enum swa_status {
  *   lse         fp32 [B, H_q, T], contiguous.
  *   row_counts  optional int32 [B, H_q, T], contiguous (NULL: not written).
  *   global_idx  optional int32 [n_global] device array of global positions, strictly
- *               increasing, each in [0, T) (NULL with n_global = 0: none).
+ *               increasing, each in [0, T) (NULL with n_global = 0: none).  The prefill
+ *               kernel checks this on the device: a list that breaks it is reported by
+ *               swa_check_device_error as SWA_ERR_INVALID_ARG (bit
+ *               SWA_DEVERR_GLOBAL_LIST); that call's outputs are then undefined, but
+ *               no memory outside its own buffers is read or written.
  *   global_mode SWA_GLOBAL_FULL (0) or SWA_GLOBAL_SINK (1): how global_idx is used.
  *   q_g, k_g, v_g  optional separate global projections, laid out like q, k, v with
  *               their own strides (all three or none; SWA_GLOBAL_FULL only).
@@ -301,10 +308,64 @@ SWA_API swa_status swa_decode_noalloc(const swa_decode_params *p, swa_stream_t s
  * Synchronises `stream`, then reads and clears the library's device error words.
  * Returns SWA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
  * call, SWA_ERR_INVALID_ARG if a kernel found device data breaking its contract
- * (a negative append position, a cache slot not holding a position a chunked
- * prefill needs), SWA_ERR_CUDA if the synchronisation failed, else SWA_OK.
+ * (a global_idx list that is not strictly increasing within [0, T), a negative
+ * append position, a cache slot not holding a position a chunked prefill needs),
+ * SWA_ERR_CUDA if the synchronisation failed, else SWA_OK.
+ * The words are per device and shared by every stream: this call synchronises only
+ * `stream`, then reads and clears them for all work on the current device.  Work
+ * still running on another stream may set them afterwards (a later call reports it),
+ * and an error raised by another stream's work is reported to whichever call reads
+ * first.  A caller that drives several streams should synchronise them all first.
  */
 SWA_API swa_status swa_check_device_error(swa_stream_t stream);
+
+/* Bits of the device error words (swa_device_errors). */
+#define SWA_DEVERR_WAIT_TIMEOUT 1u  /* prefill, split: a bounded wait expired */
+#define SWA_DEVERR_DRAIN_TIMEOUT 2u /* prefill, split: the exit path could not drain its copies in time */
+#define SWA_DEVERR_GLOBAL_LIST 4u   /* prefill: global_idx not strictly increasing within [0, T) */
+#define SWA_DEVERR_BAD_POSITION 1u  /* cache: a negative (or overflowing) append position */
+#define SWA_DEVERR_CACHE_MISMATCH 2u /* cache: a slot not holding a position a chunked prefill needs */
+
+/* The device error words, one per group of kernels. */
+typedef struct swa_device_errors {
+    uint32_t prefill; /* the band kernel of swa_fwd / swa_prefill_chunk */
+    uint32_t split;   /* decode and the global-row pass of swa_fwd (split-K and merge) */
+    uint32_t cache;   /* swa_cache_append, the history gather of swa_prefill_chunk */
+} swa_device_errors;
+
+/*
+ * As swa_check_device_error (same synchronisation, same status), and also returns the
+ * raw words it read and cleared in *out (may be NULL), for diagnosis: which group of
+ * kernels failed and how.  A wait that expired sets SWA_DEVERR_WAIT_TIMEOUT in the
+ * CTA that gave up; the other roles of that CTA then stop without a timeout of their
+ * own, and SWA_DEVERR_DRAIN_TIMEOUT means a copy or MMA was still outstanding when the
+ * CTA left (a second fault, not a consequence of the first).
+ */
+SWA_API swa_status swa_read_device_errors(swa_stream_t stream, swa_device_errors *out);
+
+/*
+ * Failure detection without a GPU fault (test hook; the pages have no counterpart).
+ * Makes the bounded-wait path above run on purpose: a producer that stops issuing
+ * copies, so that the waits of the kernel's other roles run out, and a shorter
+ * bound on each wait.  Nothing faults, traps or hangs: the kernel drains the copies it
+ * did issue, frees its tensor memory, returns, and the next call works normally.
+ *   band_stop_fill    the prefill kernel's K/V producer of every CTA issues no ring
+ *                     fill numbered at or past this (fills are numbered 0, 1, ... per
+ *                     CTA: K_0, V_0, K_1, V_1, ... of its units in order); -1 = off.
+ *   split_stop_stage  the producer of every CTA of the decode / global-row split pass
+ *                     emits no stage numbered at or past this (one stage per 64-slot
+ *                     chunk streamed, numbered per CTA); -1 = off.
+ *   wait_limit_ns     bound on each in-kernel wait, in ns; 0 = the default (2^31 ns).
+ * The plan is process-wide and read by every launch that follows; NULL (or -1, -1, 0)
+ * restores normal operation.  Outputs of a call that hit a planted stop are undefined.
+ * Returns SWA_ERR_INVALID_ARG for a stop below -1 or a negative limit.
+ */
+typedef struct swa_debug_faults {
+    int32_t band_stop_fill;
+    int32_t split_stop_stage;
+    int64_t wait_limit_ns;
+} swa_debug_faults;
+SWA_API swa_status swa_debug_set_faults(const swa_debug_faults *f);
 
 /*
  * Description of the CUDA error behind the most recent SWA_ERR_CUDA returned to the

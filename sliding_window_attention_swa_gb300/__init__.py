@@ -22,6 +22,7 @@ __all__ = [
     "swa_check_device_error", "swa_status_string", "swa_abi_version",
     "SwaFwdParams", "SwaDecodeParams", "GLOBAL_FULL", "GLOBAL_SINK",
     "SwaCacheParams", "SwaChunkParams", "swa_cache_append", "swa_decode_append", "swa_prefill_chunk",
+    "SwaDeviceErrors", "SwaDebugFaults", "swa_read_device_errors", "swa_debug_set_faults",
 ]
 
 _c_i64x3 = ctypes.c_int64 * 3
@@ -76,6 +77,26 @@ class SwaChunkParams(ctypes.Structure):
         ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("row_counts", ctypes.c_void_p), ("append", ctypes.c_int32),
     ]
 
+
+class SwaDeviceErrors(ctypes.Structure):
+    """Mirror of ``swa_device_errors`` in include/swa.h."""
+
+    _fields_ = [("prefill", ctypes.c_uint32), ("split", ctypes.c_uint32), ("cache", ctypes.c_uint32)]
+
+
+class SwaDebugFaults(ctypes.Structure):
+    """Mirror of ``swa_debug_faults`` in include/swa.h."""
+
+    _fields_ = [("band_stop_fill", ctypes.c_int32), ("split_stop_stage", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+
+# bits of the device error words
+DEVERR_WAIT_TIMEOUT = 1
+DEVERR_DRAIN_TIMEOUT = 2
+DEVERR_GLOBAL_LIST = 4
+DEVERR_BAD_POSITION = 1
+DEVERR_CACHE_MISMATCH = 2
 
 GLOBAL_FULL = 0  # global tokens: full rows and columns
 GLOBAL_SINK = 1  # attention sinks: key columns only, never right of a row's band
@@ -135,6 +156,10 @@ def load_library(path: str | None = None):
     lib.swa_prefill_chunk.restype = ctypes.c_int
     lib.swa_check_device_error.argtypes = [vp]
     lib.swa_check_device_error.restype = ctypes.c_int
+    lib.swa_read_device_errors.argtypes = [vp, ctypes.POINTER(SwaDeviceErrors)]
+    lib.swa_read_device_errors.restype = ctypes.c_int
+    lib.swa_debug_set_faults.argtypes = [ctypes.POINTER(SwaDebugFaults)]
+    lib.swa_debug_set_faults.restype = ctypes.c_int
     lib.swa_last_error_string.argtypes = []
     lib.swa_last_error_string.restype = ctypes.c_char_p
     lib.swa_status_string.argtypes = [ctypes.c_int]
@@ -439,7 +464,27 @@ def swa_prefill_chunk(q, k_new, v_new, k_cache, v_cache, slot_pos, p0, window: i
 
 
 def swa_check_device_error(stream=None) -> None:
-    """Synchronise the stream and raise if a kernel gave up on a bounded wait."""
+    """Synchronise the stream and raise if a kernel gave up on a bounded wait or found
+    device data breaking its contract."""
     st = load_library().swa_check_device_error(_stream_handle(stream))
     if st != 0:
         raise SwaError("swa_check_device_error", st)
+
+
+def swa_read_device_errors(stream=None) -> tuple[int, dict]:
+    """Synchronise the stream, read and clear the device error words: (status, words)
+    with words = {"prefill": bits, "split": bits, "cache": bits}."""
+    e = SwaDeviceErrors()
+    st = load_library().swa_read_device_errors(_stream_handle(stream), ctypes.byref(e))
+    return int(st), {"prefill": int(e.prefill), "split": int(e.split), "cache": int(e.cache)}
+
+
+def swa_debug_set_faults(band_stop_fill: int = -1, split_stop_stage: int = -1, wait_limit_ns: int = 0) -> None:
+    """Failure-detection test hook (process-wide): the prefill kernel's producer stops
+    before ring fill band_stop_fill, the split pass's before stage split_stop_stage
+    (-1: off), and each in-kernel wait is bounded by wait_limit_ns (0: the default).
+    Called with no arguments it restores normal operation."""
+    f = SwaDebugFaults(int(band_stop_fill), int(split_stop_stage), int(wait_limit_ns))
+    st = load_library().swa_debug_set_faults(ctypes.byref(f))
+    if st != 0:
+        raise SwaError("swa_debug_set_faults", st)

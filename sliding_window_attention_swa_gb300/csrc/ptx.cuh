@@ -18,9 +18,12 @@ namespace swa {
 enum : uint32_t {
     kErrWaitTimeout = 1u,   // an mbarrier / pipeline wait exceeded its limit
     kErrDrainTimeout = 2u,  // the exit path could not drain copies or MMAs in time
+    kErrBadGlobalList = 4u, // the global-position list is not strictly increasing within range
 };
 
-// Upper bound on any single wait inside a kernel, in ns of %globaltimer (~2.1 s).
+// Default upper bound on any single wait inside a kernel, in ns of %globaltimer
+// (~2.1 s).  Launches pass their bound as a kernel argument (a failure-detection test
+// shortens it).
 constexpr uint64_t kWaitLimitNs = 1ull << 31;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -82,11 +85,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // sub-partition; a suspended try_wait can wake late); otherwise poll with
 // try_wait, which lets the warp sleep and leaves issue slots to its neighbours.
 // Gives up (returns false) when *abort becomes non-zero (another role of the CTA
-// gave up) or after kWaitLimitNs, in which case it raises *abort and ORs
+// gave up) or after `limit` ns, in which case it raises *abort and ORs
 // kErrWaitTimeout into err.
 template <bool kSpin = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned int *err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, unsigned int *err,
+                                          uint64_t limit) {
     if constexpr (kSpin) {
 #pragma unroll 1
         for (int i = 0; i < 4096; ++i)
@@ -101,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             *abort = 1;
             atomicOr(err, kErrWaitTimeout);
             return false;
@@ -109,12 +112,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Exit-path wait: bounded, never raises *abort, records kErrDrainTimeout on expiry.
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, unsigned int *err) {
+// Exit-path wait: bounded by `limit` ns, never raises *abort, records kErrDrainTimeout
+// on expiry.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, unsigned int *err, uint64_t limit) {
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             atomicOr(err, kErrDrainTimeout);
             return false;
         }

@@ -1,5 +1,7 @@
 // swa_abi.cu -- the extern "C" entry points of libswa.so: argument validation on
 // the host, workspace sizing, and the kernel launches on the caller's stream.
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -18,6 +20,12 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
 constexpr float kLog2e = 1.4426950408889634f;
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Planted faults (swa_debug_set_faults); INT_MAX / 0 = off.
+std::atomic<int> g_band_stop{INT_MAX};
+std::atomic<int> g_split_stop{INT_MAX};
+std::atomic<long long> g_wait_limit{0};
+constexpr uint64_t kDefaultWaitLimitNs = 1ull << 31;
 
 // Records a failed CUDA call for swa_last_error_string(); true if `e` is a failure.
 bool failed(cudaError_t e) {
@@ -234,6 +242,15 @@ cudaError_t launch_band_views(const swa_fwd_params *p, const swa::BandArgs &base
 }
 
 }  // namespace
+
+swa::FaultPlan swa::fault_plan() {
+    FaultPlan f;
+    f.band_stop_fill = g_band_stop.load(std::memory_order_relaxed);
+    f.split_stop_stage = g_split_stop.load(std::memory_order_relaxed);
+    const long long lim = g_wait_limit.load(std::memory_order_relaxed);
+    f.wait_limit_ns = lim > 0 ? static_cast<uint64_t>(lim) : kDefaultWaitLimitNs;
+    return f;
+}
 
 swa_status swa::validate_decode(const swa_decode_params *p) { return decode_check(p); }
 bool swa::record_cuda_failure(cudaError_t e) { return failed(e); }
@@ -581,12 +598,29 @@ swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_params *
     return SWA_OK;
 }
 
-swa_status swa_check_device_error(swa_stream_t stream) {
+swa_status swa_read_device_errors(swa_stream_t stream, swa_device_errors *out) {
+    if (out) *out = swa_device_errors{};
     if (failed(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)))) return SWA_ERR_CUDA;
-    const unsigned int e = swa::band_read_clear_error() | swa::split_read_clear_error();
-    const unsigned int c = swa::cache_read_clear_error();
-    if (e) return SWA_ERR_TIMEOUT;
-    return c ? SWA_ERR_INVALID_ARG : SWA_OK;
+    swa_device_errors e;
+    e.prefill = swa::band_read_clear_error();
+    e.split = swa::split_read_clear_error();
+    e.cache = swa::cache_read_clear_error();
+    if (out) *out = e;
+    constexpr uint32_t kTimeout = SWA_DEVERR_WAIT_TIMEOUT | SWA_DEVERR_DRAIN_TIMEOUT;
+    if ((e.prefill | e.split) & kTimeout) return SWA_ERR_TIMEOUT;
+    if ((e.prefill & SWA_DEVERR_GLOBAL_LIST) || e.cache) return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+swa_status swa_check_device_error(swa_stream_t stream) { return swa_read_device_errors(stream, nullptr); }
+
+swa_status swa_debug_set_faults(const swa_debug_faults *f) {
+    if (f && (f->band_stop_fill < -1 || f->split_stop_stage < -1 || f->wait_limit_ns < 0))
+        return SWA_ERR_INVALID_ARG;
+    g_band_stop.store(f && f->band_stop_fill >= 0 ? f->band_stop_fill : INT_MAX, std::memory_order_relaxed);
+    g_split_stop.store(f && f->split_stop_stage >= 0 ? f->split_stop_stage : INT_MAX, std::memory_order_relaxed);
+    g_wait_limit.store(f ? static_cast<long long>(f->wait_limit_ns) : 0, std::memory_order_relaxed);
+    return SWA_OK;
 }
 
 }  // extern "C"

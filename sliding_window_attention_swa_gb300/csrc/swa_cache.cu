@@ -18,6 +18,8 @@ namespace {
 __device__ unsigned int g_cache_err = 0;
 constexpr unsigned int kErrBadPosition = 1u;    // a negative (or overflowing) position
 constexpr unsigned int kErrCacheMismatch = 2u;  // a slot not holding the position needed
+static_assert(kErrBadPosition == SWA_DEVERR_BAD_POSITION && kErrCacheMismatch == SWA_DEVERR_CACHE_MISMATCH,
+              "device error bits");
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;  // independent 16-byte loads in flight per thread

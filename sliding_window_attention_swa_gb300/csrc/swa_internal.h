@@ -193,4 +193,14 @@ cudaError_t run_decode(const swa_decode_params *p, void *ws, cudaStream_t s, con
 bool record_cuda_failure(cudaError_t e);                  // true (and recorded) if e failed
 unsigned int band_read_clear_error();
 
+// Planted faults of the failure-detection tests (swa_debug_set_faults), read by every
+// band and split launch: a producer that stops issuing copies (INT_MAX: off) and the
+// bound on each in-kernel wait.
+struct FaultPlan {
+    int band_stop_fill;
+    int split_stop_stage;
+    uint64_t wait_limit_ns;
+};
+FaultPlan fault_plan();
+
 }  // namespace swa

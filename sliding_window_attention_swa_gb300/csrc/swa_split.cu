@@ -86,6 +86,10 @@ struct StreamKernelArgs {
     SplitArgs s;
     int n_items;
     int nqb;
+    uint64_t wait_limit_ns;  // bound on every wait, in ns of %globaltimer
+    // planted fault of the failure-detection tests: the producer of every CTA emits no
+    // stage numbered at or past this (INT_MAX: off), so the consumers' waits run out
+    int fault_stop_stage;
 };
 
 // Registers: two 5-warp CTAs put three warps on two of the SM's sub-partitions,
@@ -206,9 +210,13 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
             for (int c = 0; c < MAX_CHUNKS && ok; ++c) {
                 const bool emit = mask[c] != 0 || (last_c < 0 && c == 0);
                 if (!emit) continue;
+                if (seq >= ka.fault_stop_stage) {  // planted fault: this stage is never emitted
+                    ok = false;
+                    break;
+                }
                 const int st = seq % NST;
                 if (seq >= NST) {
-                    ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
+                    ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err, ka.wait_limit_ns));
                     if (!ok) break;
                 }
                 if (si_new >= 0 && c == si_new / CH) {
@@ -253,7 +261,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
         }
         if (!ok && lane == 0) {
             // drain the copies still in flight (at most the last NST stages)
-            for (int s = max(0, seq - NST); s < seq; ++s) mbar_drain(bar_full(s % NST), (s / NST) & 1, &g_split_err);
+            for (int s = max(0, seq - NST); s < seq; ++s) mbar_drain(bar_full(s % NST), (s / NST) & 1, &g_split_err, ka.wait_limit_ns);
         }
     } else {
         // ============================ consumers ============================
@@ -269,7 +277,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 #pragma unroll 1
         for (int seq = 0; ok; ++seq) {
             const int st = seq % NST;
-            if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_full(st), (seq / NST) & 1, abort, &g_split_err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_full(st), (seq / NST) & 1, abort, &g_split_err, ka.wait_limit_ns))) {
                 ok = false;
                 break;
             }
@@ -409,7 +417,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                     ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
                     ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
                 }
-                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_cd, (n_done - 1) & 1, abort, &g_split_err))) {
+                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_cd, (n_done - 1) & 1, abort, &g_split_err, ka.wait_limit_ns))) {
                     ok = false;
                     break;
                 }
@@ -433,7 +441,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_cf);
-                if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_cf, n_done & 1, abort, &g_split_err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_cf, n_done & 1, abort, &g_split_err, ka.wait_limit_ns))) {
                     ok = false;
                     break;
                 }
@@ -595,6 +603,9 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
     StreamKernelArgs ka{};
     ka.s = a;
     ka.nqb = (a.NQ + a.q_per_cta - 1) / a.q_per_cta;
+    const FaultPlan fp = fault_plan();
+    ka.wait_limit_ns = fp.wait_limit_ns;
+    ka.fault_stop_stage = fp.split_stop_stage;
     const long long items = static_cast<long long>(a.B) * a.H_kv * ka.nqb * a.n_splits;
     if (items <= 0 || items > 0x7fffffffLL) return cudaErrorInvalidValue;
     ka.n_items = static_cast<int>(items);

@@ -43,7 +43,8 @@ def test_version_and_status_strings(lib):
 def test_struct_layout_matches_header(tmp_path):
     # The C compiler's sizeof / offsetof of every field against the ctypes mirrors.
     structs = {"swa_fwd_params": swa.SwaFwdParams, "swa_decode_params": swa.SwaDecodeParams,
-               "swa_cache_params": swa.SwaCacheParams, "swa_chunk_params": swa.SwaChunkParams}
+               "swa_cache_params": swa.SwaCacheParams, "swa_chunk_params": swa.SwaChunkParams,
+               "swa_device_errors": swa.SwaDeviceErrors, "swa_debug_faults": swa.SwaDebugFaults}
     lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "swa.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -223,3 +224,24 @@ def test_prefill_chunk_workspace(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         swa.load_library(str(tmp_path / "nope.so"))
+
+
+def test_debug_fault_plan_arguments(lib):
+    """The failure-detection hook takes -1 (off) or a fill / stage number and a
+    non-negative wait bound; anything else is rejected on the host."""
+    F = swa.SwaDebugFaults
+    try:
+        for bad in (F(-2, -1, 0), F(-1, -5, 0), F(-1, -1, -1)):
+            assert lib.swa_debug_set_faults(ctypes.byref(bad)) == 1
+        for good in (F(-1, -1, 0), F(0, 3, 1000000), F(12, -1, 0)):
+            assert lib.swa_debug_set_faults(ctypes.byref(good)) == 0
+        assert lib.swa_debug_set_faults(None) == 0
+    finally:
+        swa.swa_debug_set_faults()
+
+
+def test_device_error_bits_match_header():
+    """The Python constants mirror the header's SWA_DEVERR_* bits."""
+    text = open(HEADER).read()
+    bits = dict(re.findall(r"#define SWA_(DEVERR_\w+) (\d+)u", text))
+    assert bits and all(getattr(swa, k) == int(v) for k, v in bits.items())

@@ -23,6 +23,7 @@ Five build flavours are covered:
   one query tile     one barrier per fill + value releases        (globals)
 A model of the protocol, not of the kernel's code: the parity functions below restate the
 kernel's arithmetic so that a change to the ordering has to be reflected here as well."""
+import copy
 import random
 
 import pytest
@@ -255,14 +256,46 @@ class Ring:
         self.i += 1
         return True
 
-    def run(self):
+    def run(self, drain_checks=0.0, drain_back=None):
+        """drain_checks: probability, per scheduling round, of checking the exit-path drain
+        as if the producer stopped there (drain_back: how many fills back it looks)."""
         agents = [self.producer_step, self.land_one, self.release_one, self.mma_step]
         while self.i < len(self.ops) or self.g < self.nfill or self.inflight or self.releases:
+            if drain_checks and self.rng.random() < drain_checks:
+                self.check_drain(drain_back)
             order = agents[:]
             self.rng.shuffle(order)
             if not any(a() for a in order):
                 raise AssertionError(f"deadlock: units={self.units} ns={self.ns} g={self.g} op={self.ops[self.i]}")
         assert all(v == 0 for v in self.arm.values())
+
+    # ---- exit path: the producer stops after issuing fills 0 .. g-1
+    def drain_set(self, back):
+        """The barriers the kernel's producer drains: owners among fills g-back .. g-1
+        (paired: key fills and the CTA's last fill), each with the parity of that fill."""
+        lo = max(0, self.g - back)
+        if self.paired:
+            return [q for q in range(lo, self.g) if q % 2 == 0 or q + 1 == self.nfill]
+        return list(range(lo, self.g))
+
+    def check_drain(self, back=None):
+        """Every copy still in flight must be covered by the drain, and once they have all
+        landed each drain wait must name the newest completed phase of its barrier (an
+        older one would alias on parity and wait until its time limit)."""
+        ns = self.ns
+        back = ns if back is None else back
+        d = self.drain_set(back)
+        missing = {own for _, own in self.inflight} - set(d)
+        assert not missing, f"copies on barriers of fills {sorted(missing)} in flight, not drained (g={self.g})"
+        sim = copy.deepcopy(self)
+        while sim.land_one():
+            pass
+        for q in d:
+            if sim.paired:
+                ok = sim.full[q % ns].check_wait(own_ord(q, ns), fpar(q, ns))
+            else:
+                ok = sim.full[q % ns].check_wait(q // ns, (q // ns) & 1)
+            assert ok, f"drain of fill {q} names a phase that never completes"
 
 
 FLAVOURS = [
@@ -327,5 +360,31 @@ def test_model_catches_an_early_release():
             Early([12, 9, 14], 5, 2, True, "key", random.Random(seed)).run()
         except AssertionError as e:
             assert "overwrites" in str(e), e
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("nqt,paired,release,rings", FLAVOURS)
+def test_drain_after_a_stop(nqt, paired, release, rings):
+    """The exit path of the producer (a bounded wait gave up elsewhere, or a planted stop):
+    at random points of random runs, the fills g-NSLOT .. g-1 hold every copy in flight,
+    one per slot, and draining them names each barrier's newest phase."""
+    rng = random.Random(4321 + 10 * nqt + (1 if paired else 0))
+    mixes = [[1], [2, 3], [6, 7, 5], [18, 18]] + [[rng.randint(1, 30) for _ in range(rng.randint(1, 4))]
+                                                    for _ in range(25)]
+    for ns in rings:
+        for units in mixes:
+            Ring(units, ns, nqt, paired, release, rng).run(drain_checks=0.05)
+
+
+def test_model_catches_a_drain_window_one_fill_too_long():
+    """Looking NSLOT + 1 fills back, an even ring drains two key fills of one slot: the
+    older one's parity names a phase that has been overtaken (a false drain timeout)."""
+    caught = 0
+    for seed in range(20):
+        try:
+            Ring([18, 18], 12, 2, True, "key", random.Random(seed)).run(drain_checks=0.2, drain_back=13)
+        except AssertionError as e:
+            assert "aliasing" in str(e) or "never completes" in str(e), e
             caught += 1
     assert caught > 0
