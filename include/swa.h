@@ -294,8 +294,9 @@ SWA_API swa_status swa_prefill_chunk(const swa_chunk_params *p, const swa_cache_
  * compiled into the library; every GPU that loads the library holds that array until
  * the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
  * library routine is called.  The first call on each device looks up the array's
- * device address (with that device current) and caches it, so make that first call
- * before any stream capture.  All calls on a device share the array and it keeps the
+ * device address (with that device current) and caches it for the current CUDA
+ * context, so make that first call before any stream capture -- and again first after
+ * a device reset, whose new context holds the array at a new address.  All calls on a device share the array and it keeps the
  * previous call's contents (no part of it needs to start at zero); calls that overlap
  * on the GPU -- on different streams or host threads -- race on it and must be
  * serialised by the caller.  Parameters, layouts and results are those of swa_decode.
@@ -346,24 +347,22 @@ SWA_API swa_status swa_read_device_errors(swa_stream_t stream, swa_device_errors
 /*
  * Failure detection without a GPU fault (test hook; the pages have no counterpart).
  * Makes the bounded-wait path above run on purpose: a producer that stops issuing
- * copies, so that the waits of the kernel's other roles run out, and a shorter
- * bound on each wait.  Nothing faults, traps or hangs: the kernel drains the copies it
- * did issue, frees its tensor memory, returns, and the next call works normally.
+ * copies, so that the waits of the kernel's other roles run out (after the fixed bound
+ * of about 2.1 s).  Nothing faults, traps or hangs: the kernel drains the copies it did
+ * issue, frees its tensor memory, returns, and the next call works normally.
  *   band_stop_fill    the prefill kernel's K/V producer of every CTA issues no ring
  *                     fill numbered at or past this (fills are numbered 0, 1, ... per
  *                     CTA: K_0, V_0, K_1, V_1, ... of its units in order); -1 = off.
  *   split_stop_stage  the producer of every CTA of the decode / global-row split pass
  *                     emits no stage numbered at or past this (one stage per 64-slot
  *                     chunk streamed, numbered per CTA); -1 = off.
- *   wait_limit_ns     bound on each in-kernel wait, in ns; 0 = the default (2^31 ns).
- * The plan is process-wide and read by every launch that follows; NULL (or -1, -1, 0)
+ * The plan is process-wide and read by every launch that follows; NULL (or -1, -1)
  * restores normal operation.  Outputs of a call that hit a planted stop are undefined.
- * Returns SWA_ERR_INVALID_ARG for a stop below -1 or a negative limit.
+ * Returns SWA_ERR_INVALID_ARG for a stop below -1.
  */
 typedef struct swa_debug_faults {
     int32_t band_stop_fill;
     int32_t split_stop_stage;
-    int64_t wait_limit_ns;
 } swa_debug_faults;
 SWA_API swa_status swa_debug_set_faults(const swa_debug_faults *f);
 

@@ -87,8 +87,7 @@ class SwaDeviceErrors(ctypes.Structure):
 class SwaDebugFaults(ctypes.Structure):
     """Mirror of ``swa_debug_faults`` in include/swa.h."""
 
-    _fields_ = [("band_stop_fill", ctypes.c_int32), ("split_stop_stage", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64)]
+    _fields_ = [("band_stop_fill", ctypes.c_int32), ("split_stop_stage", ctypes.c_int32)]
 
 
 # bits of the device error words
@@ -479,12 +478,11 @@ def swa_read_device_errors(stream=None) -> tuple[int, dict]:
     return int(st), {"prefill": int(e.prefill), "split": int(e.split), "cache": int(e.cache)}
 
 
-def swa_debug_set_faults(band_stop_fill: int = -1, split_stop_stage: int = -1, wait_limit_ns: int = 0) -> None:
+def swa_debug_set_faults(band_stop_fill: int = -1, split_stop_stage: int = -1) -> None:
     """Failure-detection test hook (process-wide): the prefill kernel's producer stops
     before ring fill band_stop_fill, the split pass's before stage split_stop_stage
-    (-1: off), and each in-kernel wait is bounded by wait_limit_ns (0: the default).
-    Called with no arguments it restores normal operation."""
-    f = SwaDebugFaults(int(band_stop_fill), int(split_stop_stage), int(wait_limit_ns))
+    (-1: off).  Called with no arguments it restores normal operation."""
+    f = SwaDebugFaults(int(band_stop_fill), int(split_stop_stage))
     st = load_library().swa_debug_set_faults(ctypes.byref(f))
     if st != 0:
         raise SwaError("swa_debug_set_faults", st)

@@ -21,9 +21,9 @@ enum : uint32_t {
     kErrBadGlobalList = 4u, // the global-position list is not strictly increasing within range
 };
 
-// Default upper bound on any single wait inside a kernel, in ns of %globaltimer
-// (~2.1 s).  Launches pass their bound as a kernel argument (a failure-detection test
-// shortens it).
+// Upper bound on any single wait inside a kernel, in ns of %globaltimer (~2.1 s).  A
+// compile-time constant: a bound read at run time (a kernel argument, or shared memory
+// beside the abort flag) measured 3-6% slower on the prefill kernel.
 constexpr uint64_t kWaitLimitNs = 1ull << 31;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -85,11 +85,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // sub-partition; a suspended try_wait can wake late); otherwise poll with
 // try_wait, which lets the warp sleep and leaves issue slots to its neighbours.
 // Gives up (returns false) when *abort becomes non-zero (another role of the CTA
-// gave up) or after `limit` ns, in which case it raises *abort and ORs
+// gave up) or after kWaitLimitNs, in which case it raises *abort and ORs
 // kErrWaitTimeout into err.
 template <bool kSpin = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, unsigned int *err,
-                                          uint64_t limit) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned int *err) {
     if constexpr (kSpin) {
 #pragma unroll 1
         for (int i = 0; i < 4096; ++i)
@@ -104,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > limit) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
             atomicOr(err, kErrWaitTimeout);
             return false;
@@ -112,13 +112,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Exit-path wait: bounded by `limit` ns, never raises *abort, records kErrDrainTimeout
-// on expiry.
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, unsigned int *err, uint64_t limit) {
+// Exit-path wait: bounded, never raises *abort, records kErrDrainTimeout on expiry.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, unsigned int *err) {
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > limit) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, kErrDrainTimeout);
             return false;
         }

@@ -24,8 +24,6 @@ thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 // Planted faults (swa_debug_set_faults); INT_MAX / 0 = off.
 std::atomic<int> g_band_stop{INT_MAX};
 std::atomic<int> g_split_stop{INT_MAX};
-std::atomic<long long> g_wait_limit{0};
-constexpr uint64_t kDefaultWaitLimitNs = 1ull << 31;
 
 // Records a failed CUDA call for swa_last_error_string(); true if `e` is a failure.
 bool failed(cudaError_t e) {
@@ -247,8 +245,6 @@ swa::FaultPlan swa::fault_plan() {
     FaultPlan f;
     f.band_stop_fill = g_band_stop.load(std::memory_order_relaxed);
     f.split_stop_stage = g_split_stop.load(std::memory_order_relaxed);
-    const long long lim = g_wait_limit.load(std::memory_order_relaxed);
-    f.wait_limit_ns = lim > 0 ? static_cast<uint64_t>(lim) : kDefaultWaitLimitNs;
     return f;
 }
 
@@ -615,11 +611,9 @@ swa_status swa_read_device_errors(swa_stream_t stream, swa_device_errors *out) {
 swa_status swa_check_device_error(swa_stream_t stream) { return swa_read_device_errors(stream, nullptr); }
 
 swa_status swa_debug_set_faults(const swa_debug_faults *f) {
-    if (f && (f->band_stop_fill < -1 || f->split_stop_stage < -1 || f->wait_limit_ns < 0))
-        return SWA_ERR_INVALID_ARG;
+    if (f && (f->band_stop_fill < -1 || f->split_stop_stage < -1)) return SWA_ERR_INVALID_ARG;
     g_band_stop.store(f && f->band_stop_fill >= 0 ? f->band_stop_fill : INT_MAX, std::memory_order_relaxed);
     g_split_stop.store(f && f->split_stop_stage >= 0 ? f->split_stop_stage : INT_MAX, std::memory_order_relaxed);
-    g_wait_limit.store(f ? static_cast<long long>(f->wait_limit_ns) : 0, std::memory_order_relaxed);
     return SWA_OK;
 }
 

@@ -136,8 +136,6 @@ struct BandKernelArgs {
     // at most kNarrow global positions: their one column tile is kNarrow keys wide (S with
     // N = kNarrow, P V with K = kNarrow, a kNarrow-column softmax) instead of BN
     int gcol_narrow;
-    // bound on every wait, in ns of %globaltimer
-    uint64_t wait_limit_ns;
     // planted fault of the failure-detection tests: the K/V producer of every CTA issues
     // no ring fill numbered at or past this (INT_MAX: off), so the other roles' waits run out
     int fault_stop_fill;
@@ -180,8 +178,8 @@ __device__ __forceinline__ Unit unit_of(int u, const BandKernelArgs &a) {
 
 // Every lane waits (each acquires the barrier); the warp proceeds only if all did,
 // so the .sync.aligned tcgen05 instructions that follow stay convergent.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t limit) {
-    const bool ok = mbar_wait(bar, parity, abort, &g_band_err, limit);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, abort, &g_band_err);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -322,10 +320,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const int prev = p - NSLOT;
                 if constexpr (NQT == 1) {
                     const int vp = (prev & 1) ? prev : prev + 1;  // value fills release
-                    return warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort, a.wait_limit_ns);
+                    return warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
                 } else {
                     const int kp = (prev & 1) ? prev + 1 : prev;  // key fills release
-                    return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort, a.wait_limit_ns);
+                    return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
                 }
             };
             auto copy = [&](const Unit &w, int j, bool is_v, int slot, uint32_t bar) {
@@ -339,6 +337,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             int u = blockIdx.x, j = 0;
             Unit w{};
             if (u < a.n_units) w = unit_of<NQT, BN>(u, a);
+            // planted fault: only the steps whose fills all lie below a.fault_stop_fill run
+            // (step t issues fills up to 2t + 2; the last step, fill nfill - 1 alone)
+            const int n_steps = a.fault_stop_fill >= nfill ? cta_tiles : max(0, (a.fault_stop_fill - 1) / 2);
             const bool k0 = nfill > 0 && a.fault_stop_fill > 0;
             if (k0 && lane == 0) {  // K_0 alone
                 mbar_arrive_expect_tx(bar_full(0), C::TBYTES);
@@ -346,9 +347,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             }
             __syncwarp();
             g = k0 ? 1 : 0;
-            ok = nfill == 0 || k0;
+            ok = n_steps == cta_tiles;
 #pragma unroll 1
-            for (int t = 0; t < cta_tiles && ok; ++t) {
+            for (int t = 0; t < n_steps; ++t) {
                 // the tile after (u, j), possibly the next unit's first
                 int u2 = u, j2 = j + 1;
                 if (j2 >= w.n_tiles) {
@@ -358,12 +359,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const bool has_next = t + 1 < cta_tiles;
                 const Unit w2 = has_next && u2 != u ? unit_of<NQT, BN>(u2, a) : w;
                 const int pv = 2 * t + 1, own = has_next ? pv + 1 : pv;
-                if (own >= a.fault_stop_fill) {  // planted fault: these fills are never issued
+                if (!(slot_free(pv) && (!has_next || slot_free(own)))) {
                     ok = false;
                     break;
                 }
-                ok = slot_free(pv) && (!has_next || slot_free(own));
-                if (!ok) break;
                 if (lane == 0) {
                     const uint32_t bar = bar_full(own % NSLOT);
                     mbar_arrive_expect_tx(bar, (has_next ? 2u : 1u) * C::TBYTES);
@@ -384,7 +383,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 // g - 1 -- one per slot -- can be in flight; their owners are the key fills
                 // among them, and the CTA's last fill, which owns its own barrier.
                 for (int q = max(0, g - NSLOT); q < g; ++q)
-                    if ((q & 1) == 0 || q + 1 == nfill) mbar_drain(bar_full(q % NSLOT), fpar(q), &g_band_err, a.wait_limit_ns);
+                    if ((q & 1) == 0 || q + 1 == nfill) mbar_drain(bar_full(q % NSLOT), fpar(q), &g_band_err);
             }
         } else {
 #pragma unroll 1
@@ -401,13 +400,13 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         if constexpr (NQT == 1) {
                             // the slot's last fill, or (a key fill) the value fill of its tile
                             const int prev = g - NSLOT, vp = (prev & 1) ? prev : prev + 1;
-                            ok = warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort, a.wait_limit_ns);
+                            ok = warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
                         } else if constexpr (kKeyRel) {
                             // the slot's last fill, or (a value fill) the key fill of the next tile
                             const int prev = g - NSLOT, kp = (prev & 1) ? prev + 1 : prev;
-                            ok = warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort, a.wait_limit_ns);
+                            ok = warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
                         } else {
-                            ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort, a.wait_limit_ns);
+                            ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
                         }
                     }
                     if (!ok) break;
@@ -459,7 +458,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             }
             if (!ok && lane == 0) {
                 // drain the copies still in flight (at most the last NSLOT fills) before exit
-                for (int i = max(0, g - NSLOT); i < g; ++i) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err, a.wait_limit_ns);
+                for (int i = max(0, g - NSLOT); i < g; ++i) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err);
             }
         }
     } else if (warp == 2) {
@@ -474,7 +473,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
             for (int x = 0; x < NQT && ok; ++x) {
                 // the previous unit's S MMAs are done with this tile's shared memory
-                if (k >= 1) ok = warp_wait(bar_qe(x), (k - 1) & 1, abort, a.wait_limit_ns);
+                if (k >= 1) ok = warp_wait(bar_qe(x), (k - 1) & 1, abort);
                 if (!ok) break;
                 if (lane == 0) {
                     const int tx = w.t0 + x * a.TQ;
@@ -495,7 +494,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         if (!ok && lane == 0) {
             // drain the last query copy of each tile before exit
             for (int x = 0; x < NQT; ++x)
-                if (issued[x] > 0) mbar_drain(bar_qf(x), (issued[x] - 1) & 1, &g_band_err, a.wait_limit_ns);
+                if (issued[x] > 0) mbar_drain(bar_qf(x), (issued[x] - 1) & 1, &g_band_err);
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
@@ -515,7 +514,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 // paired fills: a key fill owns its barrier (with V_{jg-1} on it); with two
                 // query tiles only the CTA's first key tile is waited for here (phase 0)
                 const uint32_t kpty = kPair && NQT == 1 ? fpar(fi) : static_cast<uint32_t>((fi / NSLOT) & 1);
-                if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err, a.wait_limit_ns)) return false;
+                if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
 #pragma unroll
@@ -532,16 +531,16 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             auto mma_pv = [&](int slot, int otile, int jg, uint32_t p_parity, bool wait_v, bool first,
                               bool narrow = false) -> bool {
                 const int fi = 2 * jg + 1, s = fi % NSLOT;
-                if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err, a.wait_limit_ns)) return false;
+                if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
                 if constexpr (kPair) {
                     // V_jg arrives on the barrier of the key fill after it (K_{jg+1}), if any
                     const int own = jg + 1 < cta_tiles ? fi + 1 : fi;
-                    if (wait_v && !mbar_wait(bar_full(own % NSLOT), fpar(own), abort, &g_band_err, a.wait_limit_ns)) return false;
+                    if (wait_v && !mbar_wait(bar_full(own % NSLOT), fpar(own), abort, &g_band_err)) return false;
                 } else {
-                    if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err, a.wait_limit_ns)) return false;
+                    if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
                 }
                 // the previous unit's epilogue has read this O accumulator out
-                if (first && k >= 1 && !mbar_wait(bar_of(otile), (k - 1) & 1, abort, &g_band_err, a.wait_limit_ns)) return false;
+                if (first && k >= 1 && !mbar_wait(bar_of(otile), (k - 1) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t vb = sRing + s * C::TBYTES;
 #pragma unroll
@@ -564,14 +563,14 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const int nb = kGlob ? unit_of<NQT, BN>(u, a).n_band : n;
                 auto narrow = [&](int jj) { return kGlob && a.gcol_narrow && jj >= nb; };
                 // each query tile is waited for just before its first S MMA
-                ok = mbar_wait(bar_qf(0), k & 1, abort, &g_band_err, a.wait_limit_ns);
+                ok = mbar_wait(bar_qf(0), k & 1, abort, &g_band_err);
                 if (!ok) break;
                 if constexpr (NQT == 2) {
                     // paired fills: K_J came with V_{J-1}, waited for before that tile's P V
                     ok = mma_s(0, 0, J, !kPair || J == 0, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(0));
-                        ok = mbar_wait(bar_qf(1), k & 1, abort, &g_band_err, a.wait_limit_ns);
+                        ok = mbar_wait(bar_qf(1), k & 1, abort, &g_band_err);
                     }
                     if (ok) ok = mma_s(1, 1, J, false, narrow(0));
                     if (ok) {
@@ -627,7 +626,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             }
             if (!ok) {
                 tc_commit(bar_drain);
-                mbar_drain(bar_drain, 0, &g_band_err, a.wait_limit_ns);
+                mbar_drain(bar_drain, 0, &g_band_err);
             }
         }
         __syncwarp();
@@ -662,7 +661,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 const int jg = J + j;
                 const int slot = NQT == 2 ? wg : (jg & 1);
                 const uint32_t parity = NQT == 2 ? (jg & 1) : ((jg >> 1) & 1);
-                if (!warp_wait(bar_sf(slot), parity, abort, a.wait_limit_ns)) {
+                if (!warp_wait(bar_sf(slot), parity, abort)) {
                     ok = false;
                     break;
                 }
@@ -718,7 +717,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             // right after that P V
                             if constexpr (NQT == 1) {
                                 if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), vpar(2 * (jg - 1) + 1),
-                                               abort, a.wait_limit_ns)) {
+                                               abort)) {
                                     ok = false;
                                     break;
                                 }
@@ -918,7 +917,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     // that P V (no commit of its own on the issuing thread)
                     if constexpr (NQT == 1) {
                         if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), vpar(2 * (jg - 1) + 1),
-                                       abort, a.wait_limit_ns)) {
+                                       abort)) {
                             ok = false;
                             break;
                         }
@@ -971,7 +970,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             if (!ok) break;
 
             // ---- epilogue: O is final once this tile's last P V completes
-            if (!warp_wait(bar_od(wg), k & 1, abort, a.wait_limit_ns)) {
+            if (!warp_wait(bar_od(wg), k & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -1128,7 +1127,6 @@ cudaError_t launch_band_d(const BandArgs &x, cudaStream_t s) {
     a.sep = x.sep ? 1 : 0;
     a.gcol_narrow = glob && x.n_global <= kNarrow ? 1 : 0;
     const FaultPlan fp = fault_plan();
-    a.wait_limit_ns = fp.wait_limit_ns;
     a.fault_stop_fill = fp.band_stop_fill;
     // global-column rows come from kg / vg with separate projections or a row list
     const bool gsrc = x.sep || x.gcol_list_rows;

@@ -194,12 +194,10 @@ bool record_cuda_failure(cudaError_t e);                  // true (and recorded)
 unsigned int band_read_clear_error();
 
 // Planted faults of the failure-detection tests (swa_debug_set_faults), read by every
-// band and split launch: a producer that stops issuing copies (INT_MAX: off) and the
-// bound on each in-kernel wait.
+// band and split launch: a producer that stops issuing copies (INT_MAX: off).
 struct FaultPlan {
     int band_stop_fill;
     int split_stop_stage;
-    uint64_t wait_limit_ns;
 };
 FaultPlan fault_plan();
 

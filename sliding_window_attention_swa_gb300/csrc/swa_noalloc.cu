@@ -10,6 +10,8 @@
 // library, so it allocates nothing.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "swa_internal.h"
 
 namespace {
@@ -21,23 +23,61 @@ static __device__ __align__(256) unsigned char g_decode_scratch[SWA_DECODE_NOALL
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};  // device address of g_decode_scratch, per device
+struct ScratchEntry {
+    unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+    void *ptr;                  // device address of g_decode_scratch in that context
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per
-// device (with that device current) and cached.
+// Unique ID of the calling thread's current CUDA context, 0 if it cannot be read.  The
+// library's module -- and with it the scratch array -- is loaded again, possibly at
+// another address, in a context created after a device reset, so a cached address is
+// only reused within the context it was looked up in.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device, looked up with that
+// device current the first time a context uses it, then cached for that context.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
+    ScratchEntry &c = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (id != 0 && c.ctx_id == id && c.ptr) {
+        *out = c.ptr;
+        return cudaSuccess;
     }
-    *out = g_scratch_ptr[dev];
+    // (this also makes the device's primary context current if nothing has yet)
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    c.ctx_id = current_context_id();  // 0 (unreadable) never matches: looked up again next call
+    c.ptr = p;
+    *out = p;
     return cudaSuccess;
 }
 

@@ -86,7 +86,6 @@ struct StreamKernelArgs {
     SplitArgs s;
     int n_items;
     int nqb;
-    uint64_t wait_limit_ns;  // bound on every wait, in ns of %globaltimer
     // planted fault of the failure-detection tests: the producer of every CTA emits no
     // stage numbered at or past this (INT_MAX: off), so the consumers' waits run out
     int fault_stop_stage;
@@ -216,7 +215,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 }
                 const int st = seq % NST;
                 if (seq >= NST) {
-                    ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err, ka.wait_limit_ns));
+                    ok = __all_sync(0xffffffffu, mbar_wait<true>(bar_empty(st), ((seq / NST) - 1) & 1, abort, &g_split_err));
                     if (!ok) break;
                 }
                 if (si_new >= 0 && c == si_new / CH) {
@@ -261,7 +260,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
         }
         if (!ok && lane == 0) {
             // drain the copies still in flight (at most the last NST stages)
-            for (int s = max(0, seq - NST); s < seq; ++s) mbar_drain(bar_full(s % NST), (s / NST) & 1, &g_split_err, ka.wait_limit_ns);
+            for (int s = max(0, seq - NST); s < seq; ++s) mbar_drain(bar_full(s % NST), (s / NST) & 1, &g_split_err);
         }
     } else {
         // ============================ consumers ============================
@@ -277,7 +276,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
 #pragma unroll 1
         for (int seq = 0; ok; ++seq) {
             const int st = seq % NST;
-            if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_full(st), (seq / NST) & 1, abort, &g_split_err, ka.wait_limit_ns))) {
+            if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_full(st), (seq / NST) & 1, abort, &g_split_err))) {
                 ok = false;
                 break;
             }
@@ -417,7 +416,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                     ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
                     ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
                 }
-                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_cd, (n_done - 1) & 1, abort, &g_split_err, ka.wait_limit_ns))) {
+                if (n_done > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar_cd, (n_done - 1) & 1, abort, &g_split_err))) {
                     ok = false;
                     break;
                 }
@@ -441,7 +440,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_cf);
-                if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_cf, n_done & 1, abort, &g_split_err, ka.wait_limit_ns))) {
+                if (!__all_sync(0xffffffffu, mbar_wait<true>(bar_cf, n_done & 1, abort, &g_split_err))) {
                     ok = false;
                     break;
                 }
@@ -604,7 +603,6 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
     ka.s = a;
     ka.nqb = (a.NQ + a.q_per_cta - 1) / a.q_per_cta;
     const FaultPlan fp = fault_plan();
-    ka.wait_limit_ns = fp.wait_limit_ns;
     ka.fault_stop_stage = fp.split_stop_stage;
     const long long items = static_cast<long long>(a.B) * a.H_kv * ka.nqb * a.n_splits;
     if (items <= 0 || items > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -227,13 +227,13 @@ def test_missing_library_fails_loudly(tmp_path):
 
 
 def test_debug_fault_plan_arguments(lib):
-    """The failure-detection hook takes -1 (off) or a fill / stage number and a
-    non-negative wait bound; anything else is rejected on the host."""
+    """The failure-detection hook takes -1 (off) or a fill / stage number; anything else
+    is rejected on the host."""
     F = swa.SwaDebugFaults
     try:
-        for bad in (F(-2, -1, 0), F(-1, -5, 0), F(-1, -1, -1)):
+        for bad in (F(-2, -1), F(-1, -5)):
             assert lib.swa_debug_set_faults(ctypes.byref(bad)) == 1
-        for good in (F(-1, -1, 0), F(0, 3, 1000000), F(12, -1, 0)):
+        for good in (F(-1, -1), F(0, 3), F(12, -1)):
             assert lib.swa_debug_set_faults(ctypes.byref(good)) == 0
         assert lib.swa_debug_set_faults(None) == 0
     finally:

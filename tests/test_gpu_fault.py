@@ -2,7 +2,7 @@
 
 Planted faults (swa_debug_set_faults): a producer stops issuing copies at a chosen
 fill or stage, so the waits of its kernel's other roles run out.  Nothing faults or
-hangs: each wait is bounded (50 ms here), the CTA that gives up drains the copies and
+hangs: each wait is bounded (about 2.1 s), the CTA that gives up drains the copies and
 tensor-core work it did issue, frees its tensor memory and returns.  The host then
 reads SWA_ERR_TIMEOUT with only the wait-expiry bit set (no drain expired), and a
 normal call in the same process still matches the oracle, so the context is usable.
@@ -28,7 +28,6 @@ pytestmark = pytest.mark.gpu
 
 SWA_ERR_INVALID_ARG = 1
 SWA_ERR_TIMEOUT = 4
-WAIT_LIMIT_NS = 50_000_000
 
 
 def _inputs(seed, B, T, Hq, Hkv, d):
@@ -70,7 +69,7 @@ def test_band_producer_stop_times_out_and_recovers(case):
     scale = d ** -0.5
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     gd = None if G is None else i32_dev(G)
-    swa.swa_debug_set_faults(band_stop_fill=stop, wait_limit_ns=WAIT_LIMIT_NS)
+    swa.swa_debug_set_faults(band_stop_fill=stop)
     try:
         t0 = time.time()
         swa.swa_fwd(qd, kd, vd, wl, wr, scale, gd)
@@ -80,7 +79,7 @@ def test_band_producer_stop_times_out_and_recovers(case):
         swa.swa_debug_set_faults()
     assert st == SWA_ERR_TIMEOUT, (name, st, words)
     assert words == {"prefill": swa.DEVERR_WAIT_TIMEOUT, "split": 0, "cache": 0}, (name, words)
-    assert waited < 10.0
+    assert waited < 30.0  # one bounded wait (~2.1 s) and the drain, not a hang
     # the words were cleared and the context works: the same call, normally
     st, words = swa.swa_read_device_errors()
     assert st == 0 and words == {"prefill": 0, "split": 0, "cache": 0}
@@ -89,13 +88,13 @@ def test_band_producer_stop_times_out_and_recovers(case):
 
 
 def test_stop_past_every_fill_changes_nothing():
-    """A stop beyond every CTA's last fill, with the short wait bound: SWA_OK and the
-    oracle's result (the planted-stop compare does not disturb a normal run)."""
+    """A stop beyond every CTA's last fill: SWA_OK and the oracle's result (the
+    planted-stop compare does not disturb a normal run)."""
     import sliding_window_attention_swa_gb300 as swa
 
     B, T, Hq, Hkv, d = 1, 1000, 8, 2, 128
     q, k, v = _inputs(5101, B, T, Hq, Hkv, d)
-    swa.swa_debug_set_faults(band_stop_fill=1 << 30, split_stop_stage=1 << 30, wait_limit_ns=WAIT_LIMIT_NS)
+    swa.swa_debug_set_faults(band_stop_fill=1 << 30, split_stop_stage=1 << 30)
     try:
         _fwd_checked(q, k, v, 400, 0, d ** -0.5, [3, 500], "stop past the end")
     finally:
@@ -119,7 +118,7 @@ def test_decode_producer_stop_times_out_and_recovers():
 
     q, kc, vc, pos, qpos, d = _decode_case()
     args = (to_dev(q), to_dev(kc), to_dev(vc), i32_dev(pos), i32_dev(qpos), d ** -0.5)
-    swa.swa_debug_set_faults(split_stop_stage=5, wait_limit_ns=WAIT_LIMIT_NS)
+    swa.swa_debug_set_faults(split_stop_stage=5)
     try:
         t0 = time.time()
         swa.swa_decode(*args)
@@ -129,7 +128,7 @@ def test_decode_producer_stop_times_out_and_recovers():
         swa.swa_debug_set_faults()
     assert st == SWA_ERR_TIMEOUT, (st, words)
     assert words == {"prefill": 0, "split": swa.DEVERR_WAIT_TIMEOUT, "cache": 0}, words
-    assert waited < 10.0
+    assert waited < 30.0
     o, lse, cnt = swa.swa_decode(*args, want_counts=True)
     torch.cuda.synchronize()
     swa.swa_check_device_error()
@@ -146,7 +145,7 @@ def test_global_row_pass_stop_times_out_and_recovers():
     q, k, v = _inputs(5301, B, T, Hq, Hkv, d)
     G = [0, 1500]
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
-    swa.swa_debug_set_faults(split_stop_stage=2, wait_limit_ns=WAIT_LIMIT_NS)
+    swa.swa_debug_set_faults(split_stop_stage=2)
     try:
         swa.swa_fwd(qd, kd, vd, 200, 200, d ** -0.5, i32_dev(G))
         st, words = swa.swa_read_device_errors()

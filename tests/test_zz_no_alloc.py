@@ -85,3 +85,58 @@ def test_decode_noalloc_rejects_oversized_problem():
     assert swa.swa_decode_workspace_size(p) > (16 << 20)
     status = lib.swa_decode_noalloc(ctypes.byref(p), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert status == 5  # SWA_ERR_WORKSPACE
+
+
+def _decode_at(B, Hq=16, Hkv=1, d=64, W=64):
+    """Device tensors of a decode problem whose workspace grows by one row block per sequence."""
+    import torch
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(B)
+    q = torch.randn(B, Hq, d, generator=g, device="cuda").to(torch.bfloat16)
+    kc = torch.randn(B, Hkv, W, d, generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(B, Hkv, W, d, generator=g, device="cuda").to(torch.bfloat16)
+    L = np.arange(B) * 37 % (3 * W) + 1  # a mix of part-filled and wrapped rings
+    pos = i32_dev(I.ring_slot_positions(L, W))
+    qpos = i32_dev((L - 1).astype(np.int32))
+    return q, kc, vc, pos, qpos, d ** -0.5
+
+
+def test_decode_noalloc_at_the_scratch_limit():
+    """The largest problem whose split partials fit the scratch array exactly (within one
+    sequence's share of it) runs and matches swa_decode, twice in a row; one sequence more
+    is rejected with SWA_ERR_WORKSPACE before anything is launched."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    lib = _noalloc_lib()
+    limit = 16 << 20
+
+    def need(B):
+        q = torch.empty(B, 16, 64, dtype=torch.bfloat16, device="cuda")
+        kc = torch.empty(B, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
+        pos = torch.empty(B, 64, dtype=torch.int32, device="cuda")
+        qpos = torch.empty(B, dtype=torch.int32, device="cuda")
+        lse = torch.empty(B, 16, dtype=torch.float32, device="cuda")
+        return swa.swa_decode_workspace_size(swa.decode_params(q, kc, kc, pos, qpos, 0.1, q, lse, None))
+
+    lo, hi = 1, 1 << 16  # need(lo) <= limit < need(hi)
+    assert need(lo) <= limit < need(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= limit else (lo, mid)
+    assert limit - need(lo) < need(lo + 1) - need(lo)  # within one sequence's share
+    for _ in range(2):
+        q, kc, vc, pos, qpos, scale = _decode_at(lo)
+        o_ref, lse_ref, cnt_ref = swa.swa_decode(q, kc, vc, pos, qpos, scale, want_counts=True)
+        torch.cuda.synchronize()
+        o, lse, cnt = _noalloc_call(lib, q, kc, vc, pos, qpos, scale)
+        assert_parity(to_host_f64(o), lse.cpu().numpy().astype(np.float64), cnt.cpu().numpy(),
+                      to_host_f64(o_ref), lse_ref.cpu().numpy().astype(np.float64), cnt_ref.cpu().numpy(),
+                      f"noalloc at the limit, B={lo}")
+    q, kc, vc, pos, qpos, scale = _decode_at(hi)
+    o = torch.empty_like(q)
+    lse = torch.empty(hi, 16, dtype=torch.float32, device="cuda")
+    p = swa.decode_params(q, kc, vc, pos, qpos, scale, o, lse, None)
+    status = lib.swa_decode_noalloc(ctypes.byref(p), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == 5  # SWA_ERR_WORKSPACE
