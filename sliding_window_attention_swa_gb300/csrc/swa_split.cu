@@ -499,39 +499,137 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Sum (kMax: max) of v over the block's 128 threads; every thread gets the result.
+template <bool kMax>
+__device__ __forceinline__ float block_reduce128(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = kMax ? fmaxf(v, w) : v + w;
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = kMax ? fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])) : (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();  // red is reused by the next reduction
+    return v;
+}
+
+// Integer sum over the block's 128 threads (exact), every thread gets it.
+__device__ __forceinline__ int block_sum128_int(int v, int *red) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = (red[0] + red[1]) + (red[2] + red[3]);
+    __syncthreads();
+    return v;
+}
+
+// One block per output row (b, query, head): the log-sum-exp merge of the row's splits,
+// so that the row's work is a few dependent load latencies, not one per split.
+//   At most kMergeFewSplits splits (decode): every thread loads all the (max, sum) pairs at
+//   once and derives the weights 2^(m_s - M) itself, then loads its columns' partials of
+//   all splits at once -- no block-wide reduction.
+//   More splits (the global rows of long sequences): the block's threads read the pairs in
+//   parallel and reduce them across the block; the weights go to shared memory and each
+//   thread combines its columns over the splits four loads at a time.
+constexpr int kMergeFewSplits = 8;
+constexpr int kMergeCachedSplits = 512;  // split weights kept in shared memory (more: recomputed)
+
 __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
-    // launched as a programmatic dependent of the split pass: wait for that grid's
-    // completion (and its writes) before reading the partials
+    // launched as a programmatic dependent of the pass that wrote the partials: wait for
+    // that grid's completion (and its writes) before reading them
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float red[4];
+    __shared__ int ired[4];
+    __shared__ float wsplit[kMergeCachedSplits];
     const int qs = blockIdx.x / a.H_q, h = blockIdx.x % a.H_q, b = blockIdx.y;
     const int group = a.H_q / a.H_kv, kvh = h / group;
-    const int64_t base = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * a.n_splits;
+    const int tid = threadIdx.x, ns = a.n_splits;
+    const int64_t base = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * ns;
+    const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + base;  // (max in log2 units, sum)
+    if (ns <= kMergeFewSplits) {
+        float2 v[kMergeFewSplits];
+#pragma unroll
+        for (int i = 0; i < kMergeFewSplits; ++i) v[i] = i < ns ? ml[i] : make_float2(-INFINITY, 0.f);
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMergeFewSplits; ++i) M = fmaxf(M, v[i].x);
+        float wgt[kMergeFewSplits], L = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMergeFewSplits; ++i) {
+            wgt[i] = M == -INFINITY || i >= ns ? 0.f : exp2f(v[i].x - M);
+            L += v[i].y * wgt[i];
+        }
+        const int64_t tok = a.q_tok ? a.q_tok[qs] : 0;
+        if (tok < 0 || tok >= a.tok_limit) return;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o) + static_cast<int64_t>(b) * a.o_sb + tok * a.o_st +
+                           static_cast<int64_t>(h) * a.o_sh;
+        const float inv_l = L > 0.f ? 1.f / L : 0.f;
+        for (int d = tid; d < a.D; d += blockDim.x) {
+            const float *col = a.ws_acc + base * a.D + d;
+            float x[kMergeFewSplits];
+#pragma unroll
+            for (int i = 0; i < kMergeFewSplits; ++i) x[i] = i < ns ? col[static_cast<int64_t>(i) * a.D] : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMergeFewSplits; ++i) acc += x[i] * wgt[i];
+            o[d] = __float2bfloat16_rn(acc * inv_l);
+        }
+        if (tid == 0) {
+            const float lse = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+            a.lse[static_cast<int64_t>(b) * a.lse_sb + static_cast<int64_t>(h) * a.lse_sh + tok * a.lse_st] = lse;
+            if (a.counts) {
+                const int32_t *cn = a.ws_cnt + (static_cast<int64_t>(b) * a.H_kv + kvh) * ns;
+                int c = 0;
+#pragma unroll
+                for (int i = 0; i < kMergeFewSplits; ++i) c += i < ns ? cn[i] : 0;
+                a.counts[static_cast<int64_t>(b) * a.cnt_sb + static_cast<int64_t>(h) * a.cnt_sh + tok * a.cnt_st] =
+                    c;
+            }
+        }
+        return;
+    }
     float M = -INFINITY;
-    for (int s = 0; s < a.n_splits; ++s) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
+    for (int s = tid; s < ns; s += blockDim.x) M = fmaxf(M, ml[s].x);
+    M = block_reduce128<true>(M, red);
     float L = 0.f;
-    if (M != -INFINITY)
-        for (int s = 0; s < a.n_splits; ++s) L += a.ws_ml[(base + s) * 2 + 1] * exp2f(a.ws_ml[(base + s) * 2] - M);
+    int c = 0;
+    for (int s = tid; s < ns; s += blockDim.x) {
+        const float2 v = ml[s];
+        const float wgt = M == -INFINITY ? 0.f : exp2f(v.x - M);
+        if (s < kMergeCachedSplits) wsplit[s] = wgt;
+        L += v.y * wgt;
+        if (a.counts) c += a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * ns + s];
+    }
+    L = block_reduce128<false>(L, red);  // (its barriers also publish wsplit)
+    if (a.counts) c = block_sum128_int(c, ired);
     const int64_t tok = a.q_tok ? a.q_tok[qs] : 0;
     if (tok < 0 || tok >= a.tok_limit) return;
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o) + static_cast<int64_t>(b) * a.o_sb + tok * a.o_st +
                        static_cast<int64_t>(h) * a.o_sh;
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    const float inv_l = L > 0.f ? 1.f / L : 0.f;
+    auto weight = [&](int s) { return s < kMergeCachedSplits ? wsplit[s] : exp2f(ml[s].x - M); };
+    for (int d = tid; d < a.D; d += blockDim.x) {
+        const float *col = a.ws_acc + base * a.D + d;
         float acc = 0.f;
         if (M != -INFINITY) {
-            for (int s = 0; s < a.n_splits; ++s)
-                acc += a.ws_acc[(base + s) * a.D + d] * exp2f(a.ws_ml[(base + s) * 2] - M);
-            acc /= L;
+            int s = 0;
+            for (; s + 4 <= ns; s += 4) {
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[i] = col[static_cast<int64_t>(s + i) * a.D];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc += v[i] * weight(s + i);
+            }
+            for (; s < ns; ++s) acc += col[static_cast<int64_t>(s) * a.D] * weight(s);
         }
-        o[d] = __float2bfloat16_rn(acc);
+        o[d] = __float2bfloat16_rn(acc * inv_l);
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         const float lse = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
         a.lse[static_cast<int64_t>(b) * a.lse_sb + static_cast<int64_t>(h) * a.lse_sh + tok * a.lse_st] = lse;
-        if (a.counts) {
-            int c = 0;
-            for (int s = 0; s < a.n_splits; ++s) c += a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_splits + s];
-            a.counts[static_cast<int64_t>(b) * a.cnt_sb + static_cast<int64_t>(h) * a.cnt_sh + tok * a.cnt_st] = c;
-        }
+        if (a.counts) a.counts[static_cast<int64_t>(b) * a.cnt_sb + static_cast<int64_t>(h) * a.cnt_sh + tok * a.cnt_st] = c;
     }
 }
 

@@ -166,14 +166,15 @@ BAD_LISTS = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("mode", ["full", "sink"])
 @pytest.mark.parametrize("case", BAD_LISTS, ids=[c[0] for c in BAD_LISTS])
-def test_bad_global_list_is_reported(case, mode):
+def test_bad_global_list_is_reported(case, mode, d):
     import torch
     import sliding_window_attention_swa_gb300 as swa
 
     name, G = case
-    B, T, Hq, Hkv, d = 1, 1000, 4, 2, 128
+    B, T, Hq, Hkv = 1, 1000, 4, 2
     q, k, v = _inputs(5401, B, T, Hq, Hkv, d)
     gmode = swa.GLOBAL_SINK if mode == "sink" else swa.GLOBAL_FULL
     # outputs inside guarded buffers: nothing may be written outside the views

@@ -68,6 +68,14 @@ SMALL = [
     (2, 2048, 8, 8, 256, 99, 0, None),     # one query tile per unit: 256 units of 4-5 tiles
     (2, 2048, 8, 8, 256, 0, 0, None),      # 256 units of two 64-key tiles; o_t = v_t
     (6, 1024, 8, 4, 64, 40, 40, None),     # 192 short-band units
+    # global rows at head dim 64 with grouped heads: one global-row query block of
+    # 16 rows, ragged T, causal windows, an unbounded side, several sequences
+    (1, 777, 8, 2, 64, 100, 100, [0, 5, 400, 776]),       # G = 4 x 4 globals = 16 rows, ragged T
+    (2, 1000, 8, 2, 64, 63, 0, [10, 500, 999]),          # causal window: global rows see the future
+    (1, 600, 4, 4, 64, -1, 50, [3]),                     # unbounded left side
+    (3, 2048, 2, 2, 64, 256, 256, [0, 1024, 2047]),
+    (1, 3000, 4, 1, 64, 700, 0, [1, 2999]),              # long band (per-fill releases), G = 4
+    (1, 300, 8, 2, 64, 20, 20, [0, 100, 150, 200, 299]),  # 20 rows: two query blocks
 ]
 
 
