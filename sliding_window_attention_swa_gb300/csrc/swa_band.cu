@@ -19,14 +19,14 @@
 // Roles:
 //   warp 0        K/V producer: K_0, V_0, K_1, V_1, ... of every unit into a ring of
 //                 NSLOT shared-memory slots (TMA for band tiles, plain gathers into
-//                 the same 128B-swizzled layout for global tiles).  With two query
-//                 tiles and no global positions, V_j and K_{j+1} are copied together
-//                 and signal one barrier (that of K_{j+1}'s slot): the issuing thread
-//                 then waits once per key tile, before P_A V_j, and S_A(j+1) needs no
-//                 wait of its own.  With one query tile (no global positions) the same
-//                 pairing lets the wait before S(j+1) cover V_j's P V.  Ring slots are released by key fills only (a value
-//                 fill's last reader precedes the next key fill's); in those builds the
-//                 release is an arrive by softmax warpgroup B once it sees S_B(j) done.
+//                 the same 128B-swizzled layout for global tiles).  V_j and K_{j+1} are
+//                 copied together and signal one barrier (that of K_{j+1}'s slot): with
+//                 two query tiles the issuing thread then waits once per key tile, before
+//                 P_A V_j, and S_A(j+1) needs no wait of its own; with one query tile the
+//                 wait before S(j+1) covers V_j's P V.  With two query tiles, ring slots
+//                 are released by key fills (a value fill's last reader precedes the next
+//                 key fill's); without global positions that release is an arrive by
+//                 softmax warpgroup B once it sees S_B(j) done.
 //   warp 1        TMEM owner and MMA issuer (one thread):
 //                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
@@ -226,15 +226,16 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     // (Not in the long-band build with global positions, where a unit's last value slot,
     // held across the boundary until the next unit's first key is released, cost 1.8%.)
     constexpr bool kKeyRel = NQT == 2 && !(kGlob && !kShort);
-    // kPair (no global positions): V_j and K_{j+1} are copied together on K_{j+1}'s slot
-    // barrier, so one wait covers both: before P V_A(j) with two query tiles (S_A(j+1)
-    // follows), before S(j+1) with one (P V(j) follows).  A slot barrier then completes
-    // only for key fills (and for the CTA's last value fill, which has no key fill after
-    // it): fpar(q) is the parity of owner fill q's completion.
-    constexpr bool kPair = !kGlob;
-    // kSoftRel (those builds with two query tiles): softmax warpgroup B, which waits for S_B(j) anyway,
-    // releases K_j's slot instead of a commit on the issuing thread
-    constexpr bool kSoftRel = kPair && NQT == 2;
+    // Paired fills: V_j and K_{j+1} are copied together on K_{j+1}'s slot barrier, so one
+    // wait covers both: before P V_A(j) with two query tiles (S_A(j+1) follows), before
+    // S(j+1) with one (P V(j) follows).  A slot barrier then completes only for key fills
+    // (and for the CTA's last value fill, which has no key fill after it): fpar(q) is the
+    // parity of owner fill q's completion.  A global-column tile is gathered by the
+    // producer warp: its part of a pair is counted by one plain arrival once its stores are
+    // visible to the async proxy, the TMA part by expected bytes.
+    // kSoftRel (no global positions, two query tiles): softmax warpgroup B, which waits for
+    // S_B(j) anyway, releases K_j's slot instead of a commit on the issuing thread
+    constexpr bool kSoftRel = !kGlob && NQT == 2;
     auto fpar = [&](int q) -> uint32_t {
         const int sl = q % NSLOT, i = q / NSLOT;
         const int n = NSLOT % 2 == 1 ? (i - (sl & 1) + 1) / 2 : (sl % 2 == 0 ? i : 0);
@@ -312,154 +313,125 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
         int g = 0;  // ring fills issued so far (all units)
         bool ok = true;
-        if constexpr (kPair) {
-            // a fill's slot is free once its last occupant (a key fill), or the key fill after
-            // its last occupant (a value fill), has been released
-            auto slot_free = [&](int p) -> bool {
-                if (p < NSLOT) return true;
-                const int prev = p - NSLOT;
-                if constexpr (NQT == 1) {
-                    const int vp = (prev & 1) ? prev : prev + 1;  // value fills release
-                    return warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
-                } else {
-                    const int kp = (prev & 1) ? prev + 1 : prev;  // key fills release
-                    return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
-                }
-            };
-            auto copy = [&](const Unit &w, int j, bool is_v, int slot, uint32_t bar) {
-                const int k0 = w.kv_lo + j * BN;
+        // a fill's slot is free once its last occupant (a key fill), or the key fill after
+        // its last occupant (a value fill), has been released
+        auto slot_free = [&](int p) -> bool {
+            if (p < NSLOT) return true;
+            const int prev = p - NSLOT;
+            if constexpr (NQT == 1) {
+                const int vp = (prev & 1) ? prev : prev + 1;  // value fills release
+                return warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
+            } else if constexpr (kKeyRel) {
+                const int kp = (prev & 1) ? prev + 1 : prev;  // key fills release
+                return warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
+            } else {
+                return warp_wait(bar_empty(p % NSLOT), ((p / NSLOT) - 1) & 1, abort);  // every fill
+            }
+        };
+        auto tma_tile = [&](const Unit &w, int j, bool is_v, int slot, uint32_t bar) {
+            const int k0 = w.kv_lo + j * BN;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sRing + slot * C::TBYTES + c * (BN * 128), is_v ? &tm_v : &tm_k, bar, c * 64, w.kvh,
-                                k0, w.b);
-            };
-            const int cta_tiles = count_cta_tiles(), nfill = 2 * cta_tiles;
-            int u = blockIdx.x, j = 0;
-            Unit w{};
-            if (u < a.n_units) w = unit_of<NQT, BN>(u, a);
-            // planted fault: only the steps whose fills all lie below a.fault_stop_fill run
-            // (step t issues fills up to 2t + 2; the last step, fill nfill - 1 alone)
-            const int n_steps = a.fault_stop_fill >= nfill ? cta_tiles : max(0, (a.fault_stop_fill - 1) / 2);
-            const bool k0 = nfill > 0 && a.fault_stop_fill > 0;
-            if (k0 && lane == 0) {  // K_0 alone
-                mbar_arrive_expect_tx(bar_full(0), C::TBYTES);
-                copy(w, 0, false, 0, bar_full(0));
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d(sRing + slot * C::TBYTES + c * (BN * 128), is_v ? &tm_v : &tm_k, bar, c * 64, w.kvh,
+                            k0, w.b);
+        };
+        // global-column tile: rows global_idx[g0 + r] (zero rows past the list), gathered by
+        // the warp into the 128B-swizzled layout a TMA copy would have written
+        auto gather_tile = [&](const Unit &w, int j, bool is_v, int slot) {
+            if constexpr (kGlob) {
+                const int g0 = (j - w.n_band) * BN;
+                const __nv_bfloat16 *src = is_v ? a.v : a.k;
+                const int64_t *st = is_v ? a.v_st : a.k_st;
+                constexpr int kPieces = D / 8;
+                const int rows = a.gcol_narrow ? kNarrow : BN;  // rows the MMAs read
+                for (int idx = lane; idx < rows * kPieces; idx += 32) {
+                    const int r = idx / kPieces, pc = idx % kPieces;
+                    const int gi = g0 + r;
+                    int srow = -1;
+                    if (gi < a.n_global) {
+                        if (a.gcol_list_rows) {
+                            srow = gi;
+                        } else {
+                            const int gs = a.global_idx[gi];
+                            if (gs >= 0 && gs < a.Tk) srow = gs;
+                        }
+                    }
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (srow >= 0)
+                        val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(w.b) * st[0] +
+                                                               static_cast<int64_t>(srow) * st[1] +
+                                                               static_cast<int64_t>(w.kvh) * st[2] + pc * 8);
+                    const uint32_t off = (pc >> 3) * (BN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sgen + C::OFF_RING + slot * C::TBYTES + off) = val;
+                }
+            }
+        };
+        // one barrier phase for tile (wa, ja) and, if `two`, key tile (wb, jb): band tiles by
+        // TMA (their bytes expected on the barrier), global tiles gathered by the warp, whose
+        // one arrival comes only after its stores are visible to the tensor cores
+        auto fill = [&](const Unit &wa, int ja, bool va, int sa, bool two, const Unit &wb, int jb, int sb,
+                        uint32_t bar) {
+            const bool ta = !kGlob || ja < wa.n_band, tb = two && (!kGlob || jb < wb.n_band);
+            const bool gath = !ta || (two && !tb);
+            const uint32_t tx = (ta ? 1u : 0u) + (tb ? 1u : 0u);
+            if (lane == 0) {
+                if (!gath)
+                    mbar_arrive_expect_tx(bar, tx * C::TBYTES);
+                else if (tx > 0)
+                    mbar_expect_tx(bar, tx * C::TBYTES);
+                if (ta) tma_tile(wa, ja, va, sa, bar);
+                if (tb) tma_tile(wb, jb, false, sb, bar);
+            }
+            if (gath) {
+                if (!ta) gather_tile(wa, ja, va, sa);
+                if (two && !tb) gather_tile(wb, jb, false, sb);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar);
             }
             __syncwarp();
-            g = k0 ? 1 : 0;
-            ok = n_steps == cta_tiles;
+        };
+        const int cta_tiles = count_cta_tiles(), nfill = 2 * cta_tiles;
+        int u = blockIdx.x, j = 0;
+        Unit w{};
+        if (u < a.n_units) w = unit_of<NQT, BN>(u, a);
+        // planted fault: only the steps whose fills all lie below a.fault_stop_fill run
+        // (step t issues fills up to 2t + 2; the last step, fill nfill - 1 alone)
+        const int n_steps = a.fault_stop_fill >= nfill ? cta_tiles : max(0, (a.fault_stop_fill - 1) / 2);
+        const bool k0 = nfill > 0 && a.fault_stop_fill > 0;
+        if (k0) fill(w, 0, false, 0, false, w, 0, 0, bar_full(0));  // K_0 alone
+        g = k0 ? 1 : 0;
+        ok = n_steps == cta_tiles;
 #pragma unroll 1
-            for (int t = 0; t < n_steps; ++t) {
-                // the tile after (u, j), possibly the next unit's first
-                int u2 = u, j2 = j + 1;
-                if (j2 >= w.n_tiles) {
-                    u2 = u + static_cast<int>(gridDim.x);
-                    j2 = 0;
-                }
-                const bool has_next = t + 1 < cta_tiles;
-                const Unit w2 = has_next && u2 != u ? unit_of<NQT, BN>(u2, a) : w;
-                const int pv = 2 * t + 1, own = has_next ? pv + 1 : pv;
-                if (!(slot_free(pv) && (!has_next || slot_free(own)))) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    const uint32_t bar = bar_full(own % NSLOT);
-                    mbar_arrive_expect_tx(bar, (has_next ? 2u : 1u) * C::TBYTES);
-                    copy(w, j, true, pv % NSLOT, bar);
-                    if (has_next) copy(w2, j2, false, own % NSLOT, bar);
-                }
-                __syncwarp();
-                g = own + 1;
-                u = u2;
-                j = j2;
-                w = w2;
+        for (int t = 0; t < n_steps; ++t) {
+            // the tile after (u, j), possibly the next unit's first
+            int u2 = u, j2 = j + 1;
+            if (j2 >= w.n_tiles) {
+                u2 = u + static_cast<int>(gridDim.x);
+                j2 = 0;
             }
-            if (!ok && lane == 0) {
-                // drain the owner barriers of the copies that may still be in flight.  Fills
-                // below g - NSLOT have landed: fill q + NSLOT was issued only once the key
-                // (NQT = 2) or value (NQT = 1) fill that releases q's slot was released, and
-                // its readers waited for the owner barrier of q.  So only fills g - NSLOT ..
-                // g - 1 -- one per slot -- can be in flight; their owners are the key fills
-                // among them, and the CTA's last fill, which owns its own barrier.
-                for (int q = max(0, g - NSLOT); q < g; ++q)
-                    if ((q & 1) == 0 || q + 1 == nfill) mbar_drain(bar_full(q % NSLOT), fpar(q), &g_band_err);
+            const bool has_next = t + 1 < cta_tiles;
+            const Unit w2 = has_next && u2 != u ? unit_of<NQT, BN>(u2, a) : w;
+            const int pv = 2 * t + 1, own = has_next ? pv + 1 : pv;
+            if (!(slot_free(pv) && (!has_next || slot_free(own)))) {
+                ok = false;
+                break;
             }
-        } else {
-#pragma unroll 1
-            for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                const Unit w = unit_of<NQT, BN>(u, a);
-#pragma unroll 1
-                for (int i = 0; i < 2 * w.n_tiles; ++i) {
-                    if (g >= a.fault_stop_fill) {  // planted fault: this fill is never issued
-                        ok = false;
-                        break;
-                    }
-                    const int s = g % NSLOT;
-                    if (g >= NSLOT) {
-                        if constexpr (NQT == 1) {
-                            // the slot's last fill, or (a key fill) the value fill of its tile
-                            const int prev = g - NSLOT, vp = (prev & 1) ? prev : prev + 1;
-                            ok = warp_wait(bar_empty(vp % NSLOT), vpar(vp), abort);
-                        } else if constexpr (kKeyRel) {
-                            // the slot's last fill, or (a value fill) the key fill of the next tile
-                            const int prev = g - NSLOT, kp = (prev & 1) ? prev + 1 : prev;
-                            ok = warp_wait(bar_empty(kp % NSLOT), kpar(kp), abort);
-                        } else {
-                            ok = warp_wait(bar_empty(s), ((g / NSLOT) - 1) & 1, abort);
-                        }
-                    }
-                    if (!ok) break;
-                    const int j = i >> 1;
-                    const bool is_v = (i & 1) != 0;
-                    const uint32_t dst = sRing + s * C::TBYTES;
-                    if (!kGlob || j < w.n_band) {
-                        if (lane == 0) {
-                            const int k0 = w.kv_lo + j * BN;
-                            mbar_arrive_expect_tx(bar_full(s), C::TBYTES);
-#pragma unroll
-                            for (int c = 0; c < D / 64; ++c)
-                                tma_load_4d(dst + c * (BN * 128), is_v ? &tm_v : &tm_k, bar_full(s), c * 64, w.kvh, k0,
-                                            w.b);
-                        }
-                    } else {
-                        // global-column tile: rows global_idx[g0 + r] (zero rows past the list)
-                        const int g0 = (j - w.n_band) * BN;
-                        const __nv_bfloat16 *src = is_v ? a.v : a.k;
-                        const int64_t *st = is_v ? a.v_st : a.k_st;
-                        constexpr int kPieces = D / 8;
-                        const int rows = a.gcol_narrow ? kNarrow : BN;  // rows the MMAs read
-                        for (int idx = lane; idx < rows * kPieces; idx += 32) {
-                            const int r = idx / kPieces, pc = idx % kPieces;
-                            const int gi = g0 + r;
-                            int srow = -1;
-                            if (gi < a.n_global) {
-                                if (a.gcol_list_rows) {
-                                    srow = gi;
-                                } else {
-                                    const int gs = a.global_idx[gi];
-                                    if (gs >= 0 && gs < a.Tk) srow = gs;
-                                }
-                            }
-                            uint4 val = make_uint4(0, 0, 0, 0);
-                            if (srow >= 0)
-                                val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(w.b) * st[0] +
-                                                                       static_cast<int64_t>(srow) * st[1] +
-                                                                       static_cast<int64_t>(w.kvh) * st[2] + pc * 8);
-                            const uint32_t off = (pc >> 3) * (BN * 128) + r * 128 + (((pc & 7) ^ (r & 7)) << 4);
-                            *reinterpret_cast<uint4 *>(sgen + C::OFF_RING + s * C::TBYTES + off) = val;
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_full(s));
-                    }
-                    ++g;
-                }
-            }
-            if (!ok && lane == 0) {
-                // drain the copies still in flight (at most the last NSLOT fills) before exit
-                for (int i = max(0, g - NSLOT); i < g; ++i) mbar_drain(bar_full(i % NSLOT), (i / NSLOT) & 1, &g_band_err);
-            }
+            fill(w, j, true, pv % NSLOT, has_next, w2, j2, own % NSLOT, bar_full(own % NSLOT));
+            g = own + 1;
+            u = u2;
+            j = j2;
+            w = w2;
+        }
+        if (!ok && lane == 0) {
+            // drain the owner barriers of the copies that may still be in flight.  Fills
+            // below g - NSLOT have landed: fill q + NSLOT was issued only once the key
+            // (NQT = 2) or value (NQT = 1) fill that releases q's slot was released, and
+            // its readers waited for the owner barrier of q.  So only fills g - NSLOT ..
+            // g - 1 -- one per slot -- can be in flight; their owners are the key fills
+            // among them, and the CTA's last fill, which owns its own barrier.
+            for (int q = max(0, g - NSLOT); q < g; ++q)
+                if ((q & 1) == 0 || q + 1 == nfill) mbar_drain(bar_full(q % NSLOT), fpar(q), &g_band_err);
         }
     } else if (warp == 2) {
         // ============================ Q loader ============================
@@ -507,13 +479,13 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             int J = 0;  // key tiles of this CTA's previous units
             int k = 0;  // units of this CTA so far
             int cta_tiles = 0;
-            if constexpr (kPair) cta_tiles = count_cta_tiles();
+            cta_tiles = count_cta_tiles();
             // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
             auto mma_s = [&](int slot, int qt, int jg, bool wait_k, bool narrow = false) -> bool {
                 const int fi = 2 * jg, s = fi % NSLOT;
                 // paired fills: a key fill owns its barrier (with V_{jg-1} on it); with two
                 // query tiles only the CTA's first key tile is waited for here (phase 0)
-                const uint32_t kpty = kPair && NQT == 1 ? fpar(fi) : static_cast<uint32_t>((fi / NSLOT) & 1);
+                const uint32_t kpty = NQT == 1 ? fpar(fi) : static_cast<uint32_t>((fi / NSLOT) & 1);
                 if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
@@ -532,13 +504,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                               bool narrow = false) -> bool {
                 const int fi = 2 * jg + 1, s = fi % NSLOT;
                 if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
-                if constexpr (kPair) {
-                    // V_jg arrives on the barrier of the key fill after it (K_{jg+1}), if any
-                    const int own = jg + 1 < cta_tiles ? fi + 1 : fi;
-                    if (wait_v && !mbar_wait(bar_full(own % NSLOT), fpar(own), abort, &g_band_err)) return false;
-                } else {
-                    if (wait_v && !mbar_wait(bar_full(s), (fi / NSLOT) & 1, abort, &g_band_err)) return false;
-                }
+                // V_jg arrives on the barrier of the key fill after it (K_{jg+1}), if any
+                const int own = jg + 1 < cta_tiles ? fi + 1 : fi;
+                if (wait_v && !mbar_wait(bar_full(own % NSLOT), fpar(own), abort, &g_band_err)) return false;
                 // the previous unit's epilogue has read this O accumulator out
                 if (first && k >= 1 && !mbar_wait(bar_of(otile), (k - 1) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
@@ -567,7 +535,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (!ok) break;
                 if constexpr (NQT == 2) {
                     // paired fills: K_J came with V_{J-1}, waited for before that tile's P V
-                    ok = mma_s(0, 0, J, !kPair || J == 0, narrow(0));
+                    ok = mma_s(0, 0, J, J == 0, narrow(0));
                     if (ok) {
                         tc_commit(bar_sf(0));
                         ok = mbar_wait(bar_qf(1), k & 1, abort, &g_band_err);
@@ -583,7 +551,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         ok = mma_pv(0, 0, jg, jg & 1, true, j == 0, narrow(j));
                         if (!ok) break;
                         if (j + 1 < n) {
-                            ok = mma_s(0, 0, jg + 1, !kPair, narrow(j + 1));
+                            ok = mma_s(0, 0, jg + 1, false, narrow(j + 1));
                             if (!ok) break;
                             tc_commit(bar_sf(0));
                         } else {
@@ -616,7 +584,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                             tc_commit(bar_sf((jg + 1) & 1));
                         }
                         // paired fills: V_jg came with K_{jg+1}, waited for by S(jg+1) just above
-                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, !kPair || j + 1 == n, j == 0, narrow(j));
+                        ok = mma_pv(jg & 1, 0, jg, (jg >> 1) & 1, j + 1 == n, j == 0, narrow(j));
                         if (!ok) break;
                         tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 == n) tc_commit(bar_od(0));

@@ -52,7 +52,7 @@ def _fwd_checked(q, k, v, wl, wr, scale, G, what):
 BAND = [
     # name, (B, T, Hq, Hkv, d, wl, wr), globals, stop fill
     ("paired-d128-odd-ring", (1, 2000, 8, 2, 128, 999, 0), None, 8),
-    ("per-fill-d128-globals", (1, 2000, 8, 2, 128, 999, 0), [0, 1000], 8),
+    ("paired-d128-globals", (1, 2000, 8, 2, 128, 999, 0), [0, 1000], 8),
     ("paired-d64-even-ring", (1, 4000, 4, 4, 64, 2000, 0), None, 26),
     ("paired-d256-one-tile", (1, 1500, 2, 1, 256, 1000, 0), None, 12),
     ("paired-d128-first-fill", (1, 700, 4, 2, 128, 300, 0), None, 0),

@@ -303,6 +303,7 @@ FLAVOURS = [
     (2, True, "key", (3, 4, 5, 6, 12)),
     (2, False, "key", (3, 4, 5, 6, 12)),
     (2, False, "all", (3, 4, 5, 6, 12)),
+    (2, True, "all", (3, 4, 5, 6, 12)),
     (1, True, "value", (3, 5, 7)),
     (1, False, "value", (3, 5, 7)),
 ]
