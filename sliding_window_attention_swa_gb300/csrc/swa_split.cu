@@ -53,15 +53,17 @@ struct StageHdr {
     unsigned long long pad2;
 };
 
-// Two CTAs share an SM where the shared memory allows (head dim <= 128), so one
-// CTA's end-of-item combine overlaps the other's streaming; two or more 32 KB
-// stages in flight per CTA keep HBM busy.
+// Several CTAs share an SM where shared memory and registers allow -- three at head dim
+// 64 (three 16 KB stages each), two at 128 -- so one CTA's end-of-item combine and its
+// consumers' latency-bound chains overlap the others' streaming.  (Three at d = 64 took the
+// Longformer global rows' pass, two query rows per head, from 46.6% of the DRAM peak; at
+// d = 128 a third CTA would leave one stage each.)
 template <int D>
 struct StreamCfg {
     static constexpr int STAGE = 2 * CH * D * 2;        // K + V of one chunk
     static constexpr int CROW = D + 8;  // padded row: float2 stores of 4 rows per half-warp hit distinct banks
     static constexpr int CBUF = 4 * kSplitRows * CROW * 4;  // combine buffer [4 warps][16 rows][CROW] fp32
-    static constexpr int CTAS_PER_SM = D <= 128 ? 2 : 1;
+    static constexpr int CTAS_PER_SM = D <= 64 ? 3 : D <= 128 ? 2 : 1;
     static constexpr int NST_RAW = (232448 / CTAS_PER_SM - 2048 - CBUF) / STAGE;
     static constexpr int NST = NST_RAW > 8 ? 8 : NST_RAW;
     static constexpr int OFF_RING = 0;
@@ -92,9 +94,10 @@ struct StreamKernelArgs {
 };
 
 // Registers: two 5-warp CTAs put three warps on two of the SM's sub-partitions,
-// whose 16K-register files then allow at most 168 registers a thread.
+// whose 16K-register files then allow at most 168 registers a thread; three CTAs put
+// four warps on three of them (at most 128).
 template <int D>
-__global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
+__global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>::CTAS_PER_SM == 2 ? 168 : 255)
     stream_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const StreamKernelArgs ka) {
     using C = StreamCfg<D>;
@@ -726,7 +729,11 @@ cudaError_t launch_stream_d(const SplitArgs &a, cudaStream_t s) {
 
 }  // namespace
 
-int split_grid(int D) { return sm_count() * (D <= 128 ? StreamCfg<128>::CTAS_PER_SM : StreamCfg<256>::CTAS_PER_SM); }
+int split_grid(int D) {
+    return sm_count() * (D <= 64    ? StreamCfg<64>::CTAS_PER_SM
+                         : D <= 128 ? StreamCfg<128>::CTAS_PER_SM
+                                    : StreamCfg<256>::CTAS_PER_SM);
+}
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t s) {
     switch (a.D) {
