@@ -326,6 +326,7 @@ SWA_API swa_status swa_check_device_error(swa_stream_t stream);
 #define SWA_DEVERR_GLOBAL_LIST 4u   /* prefill: global_idx not strictly increasing within [0, T) */
 #define SWA_DEVERR_BAD_POSITION 1u  /* cache: a negative (or overflowing) append position */
 #define SWA_DEVERR_CACHE_MISMATCH 2u /* cache: a slot not holding a position a chunked prefill needs */
+#define SWA_DEVERR_BOUNDS 8u         /* any word, debug library only: an index outside its tensor (access skipped) */
 
 /* The device error words, one per group of kernels. */
 typedef struct swa_device_errors {
@@ -337,7 +338,10 @@ typedef struct swa_device_errors {
 /*
  * As swa_check_device_error (same synchronisation, same status), and also returns the
  * raw words it read and cleared in *out (may be NULL), for diagnosis: which group of
- * kernels failed and how.  A wait that expired sets SWA_DEVERR_WAIT_TIMEOUT in the
+ * kernels failed and how.  SWA_DEVERR_BOUNDS is set only by the debug build of the
+ * library (libswa_debug.so, compiled with -DSWA_DEBUG), whose kernels check every
+ * computed gather, store and copy index against its tensor before the access and skip
+ * the access when the check fails; it is reported as SWA_ERR_INVALID_ARG.  A wait that expired sets SWA_DEVERR_WAIT_TIMEOUT in the
  * CTA that gave up; the other roles of that CTA then stop without a timeout of their
  * own, and SWA_DEVERR_DRAIN_TIMEOUT means a copy or MMA was still outstanding when the
  * CTA left (a second fault, not a consequence of the first).

@@ -96,6 +96,7 @@ DEVERR_DRAIN_TIMEOUT = 2
 DEVERR_GLOBAL_LIST = 4
 DEVERR_BAD_POSITION = 1
 DEVERR_CACHE_MISMATCH = 2
+DEVERR_BOUNDS = 8
 
 GLOBAL_FULL = 0  # global tokens: full rows and columns
 GLOBAL_SINK = 1  # attention sinks: key columns only, never right of a row's band
@@ -120,9 +121,10 @@ def library_path() -> str:
     return _build_mod.LIB
 
 
-def build(force: bool = False) -> str:
-    """Compile libswa.so for sm_103a (in-tree) and return its path."""
-    return _build_mod.build(force=force)
+def build(force: bool = False, debug: bool = False) -> str:
+    """Compile libswa.so for sm_103a (in-tree) and return its path; debug=True builds
+    libswa_debug.so, whose kernels check every computed index (SWA_DEVERR_BOUNDS)."""
+    return _build_mod.build(force=force, debug=debug)
 
 
 def load_library(path: str | None = None):
@@ -168,6 +170,15 @@ def load_library(path: str | None = None):
     if path is None:
         _lib = lib
     return lib
+
+
+def use_library(lib):
+    """Make `lib` (as returned by load_library(path)) the library the functions of this
+    module call -- for example the debug build -- and return the previous one (None if
+    none was loaded yet)."""
+    global _lib
+    prev, _lib = _lib, lib
+    return prev
 
 
 def swa_status_string(status: int) -> str:

@@ -18,6 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libswa.so")
+# debug build: kernels compiled with -DSWA_DEBUG (bounds checks on every computed index)
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libswa_debug.so")
 SOURCES = ["swa_abi.cu", "swa_band.cu", "swa_split.cu", "swa_noalloc.cu", "swa_cache.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,14 +44,17 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), debug: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra = ("-DSWA_DEBUG", *extra)
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "swa.h"))
     objs, jobs = [], []
     for src in SOURCES:
         sp = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [sp, *headers]):
             jobs.append([nvcc(), *flags(extra), "-c", sp, "-o", obj])
@@ -65,11 +71,11 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         for err in ex.map(run, jobs):
             if verbose and err:
                 print(err, file=sys.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

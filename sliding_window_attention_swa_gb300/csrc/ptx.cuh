@@ -21,6 +21,23 @@ enum : uint32_t {
     kErrBadGlobalList = 4u, // the global-position list is not strictly increasing within range
 };
 
+// Bounds checks of the debug build (compiled with -DSWA_DEBUG): SWA_IN_BOUNDS(cond, word)
+// checks an index computed from the arguments against the extent of the tensor it
+// addresses, before the access it guards.  When the check fails it ORs kErrBounds into
+// the kernel group's error word and returns false, so the access is skipped -- the
+// kernel never traps.  Release builds compile it to `true` (the condition is not
+// evaluated).
+constexpr uint32_t kErrBounds = 8u;
+#ifdef SWA_DEBUG
+__device__ __forceinline__ bool in_bounds_checked(bool ok, unsigned int *err) {
+    if (!ok) atomicOr(err, kErrBounds);
+    return ok;
+}
+#define SWA_IN_BOUNDS(cond, err) (::swa::in_bounds_checked((cond), (err)))
+#else
+#define SWA_IN_BOUNDS(cond, err) (true)
+#endif
+
 // Upper bound on any single wait inside a kernel, in ns of %globaltimer (~2.1 s).  A
 // compile-time constant: a bound read at run time (a kernel argument, or shared memory
 // beside the abort flag) measured 3-6% slower on the prefill kernel.

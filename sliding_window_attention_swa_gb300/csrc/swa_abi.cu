@@ -604,7 +604,8 @@ swa_status swa_read_device_errors(swa_stream_t stream, swa_device_errors *out) {
     if (out) *out = e;
     constexpr uint32_t kTimeout = SWA_DEVERR_WAIT_TIMEOUT | SWA_DEVERR_DRAIN_TIMEOUT;
     if ((e.prefill | e.split) & kTimeout) return SWA_ERR_TIMEOUT;
-    if ((e.prefill & SWA_DEVERR_GLOBAL_LIST) || e.cache) return SWA_ERR_INVALID_ARG;
+    if ((e.prefill & SWA_DEVERR_GLOBAL_LIST) || ((e.prefill | e.split) & SWA_DEVERR_BOUNDS) || e.cache)
+        return SWA_ERR_INVALID_ARG;
     return SWA_OK;
 }
 

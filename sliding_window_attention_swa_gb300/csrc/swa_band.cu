@@ -333,6 +333,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         };
         auto tma_tile = [&](const Unit &w, int j, bool is_v, int slot, uint32_t bar) {
             const int k0 = w.kv_lo + j * BN;
+            // debug build: the tile starts inside the key rows of an existing (b, kv head)
+            (void)SWA_IN_BOUNDS(k0 >= 0 && k0 < a.Tk && w.b >= 0 && w.b < a.B && w.kvh >= 0 && w.kvh < a.H_kv,
+                                &g_band_err);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
                 tma_load_4d(sRing + slot * C::TBYTES + c * (BN * 128), is_v ? &tm_v : &tm_k, bar, c * 64, w.kvh,
@@ -360,7 +363,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         }
                     }
                     uint4 val = make_uint4(0, 0, 0, 0);
-                    if (srow >= 0)
+                    if (srow >= 0 && SWA_IN_BOUNDS(srow < (a.gcol_list_rows ? a.n_global : a.Tk) && w.b < a.B &&
+                                                       w.kvh < a.H_kv && pc * 8 < D,
+                                                   &g_band_err))
                         val = *reinterpret_cast<const uint4 *>(src + static_cast<int64_t>(w.b) * st[0] +
                                                                static_cast<int64_t>(srow) * st[1] +
                                                                static_cast<int64_t>(w.kvh) * st[2] + pc * 8);
@@ -453,6 +458,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (lane == 0) {
                     const int tx = w.t0 + x * a.TQ;
                     if (tx < a.T) {
+                        // debug build: the tile's tokens and its group's heads exist
+                        (void)SWA_IN_BOUNDS(tx >= 0 && (w.kvh + 1) * a.G <= a.H_q && w.b < a.B, &g_band_err);
                         mbar_arrive_expect_tx(bar_qf(x), static_cast<uint32_t>(a.G * a.TQ * D * 2));
 #pragma unroll
                         for (int c = 0; c < D / 64; ++c)
@@ -617,8 +624,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             const Unit w = unit_of<NQT, BN>(u, a);
             const int tx = w.t0 + wg * a.TQ;  // first token of this warpgroup's query tile
             const int t = tx + tq;
-            const bool row_ok = tq < a.TQ && t < a.T;
             const int h = w.kvh * a.G + hj;
+            // (debug build: a real row's O, lse and count addresses lie inside their tensors)
+            const bool row_ok =
+                tq < a.TQ && t < a.T && SWA_IN_BOUNDS(t >= 0 && h < a.H_q && w.b < a.B, &g_band_err);
             // key-index positions of this tile's first and last rows and of this row
             const int tlo = tx + a.q_off, thi = min(a.T - 1, tx + a.TQ - 1) + a.q_off;
             const int tk = t + a.q_off;

@@ -10,6 +10,7 @@
 #include <atomic>
 #include <climits>
 
+#include "ptx.cuh"
 #include "swa_internal.h"
 
 namespace swa {
@@ -91,6 +92,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, co
             }
             const bool is_v = c >= P / 2;
             const int pc = is_v ? c - P / 2 : c;
+            // debug build: the new row and its slot exist
+            if (!SWA_IN_BOUNDS(b < a.B && i < a.n && kvh < a.H_kv && slot >= 0 && slot < a.n_slots, &g_cache_err))
+                continue;
             const int64_t src = ((static_cast<int64_t>(b) * a.n + i) * a.H_kv + kvh) * D;
             const int64_t dsto = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
             val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vn : a.kn) + src) + pc);
@@ -139,6 +143,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a, co
                 const uint32_t bq = fdiv(bx, pl.n);
                 const int xx = static_cast<int>(bx - bq * pl.n.d);
                 const int b = static_cast<int>(bq);
+                // debug build: the gathered row (b, key index, kv head) exists
+                if (!SWA_IN_BOUNDS(b < a.B && xx < Tk && kvh < a.H_kv, &g_cache_err)) continue;
                 const int64_t p0 = __ldg(a.p0 + b);
                 // history positions present right before p0 (a sink cache's ring covers the window)
                 const int64_t ring = a.n_sink == 0 ? a.n_slots : a.W - 1;
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a, co
                     const int64_t p = p0 - (a.W - 1) + xx;
                     const uint32_t pr = static_cast<uint32_t>(p - a.n_sink);
                     const int64_t slot = p < a.n_sink ? p : a.n_sink + (pr - fdiv(pr, pl.ring) * pl.ring.d);
+                    if (!SWA_IN_BOUNDS(slot >= 0 && slot < a.n_slots, &g_cache_err)) continue;
                     if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + slot) == p) {
                         const int64_t src = ((static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_slots + slot) * D;
                         val[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? a.vc : a.kc) + src) + pc);
@@ -170,6 +177,9 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const GatherArgs a, co
                 const uint32_t bq = fdiv(bs, pl.sink);
                 const int sidx = static_cast<int>(bs - bq * pl.sink.d);
                 const int b = static_cast<int>(bq);
+                // debug build: the sink row (b, sink, kv head) exists
+                if (!SWA_IN_BOUNDS(b < a.B && sidx < a.n_sink && sidx < a.n_slots && kvh < a.H_kv, &g_cache_err))
+                    continue;
                 const int64_t p0 = __ldg(a.p0 + b);
                 if (sidx < p0) {
                     if (__ldg(a.slot_pos + static_cast<int64_t>(b) * a.n_slots + sidx) == sidx) {

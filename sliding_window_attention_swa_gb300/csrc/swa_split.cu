@@ -168,6 +168,8 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
             const int b = item / (a.n_splits * Y);
             const int kvh = y / ka.nqb, qb = y % ka.nqb;
             const int slot0 = split * a.slots_per_split;
+            // debug build: the item is a (sequence, kv head, query block, split) that exists
+            (void)SWA_IN_BOUNDS(b < a.B && kvh < a.H_kv && qb < ka.nqb && slot0 < a.n_slots, &g_split_err);
             const int64_t t = a.q_pos ? static_cast<int64_t>(a.q_pos[b]) : 0;
             // decode with append: the current token goes to slot(t) before it is read;
             // si_new is that slot's index in this split (-1: not in this split)
@@ -199,9 +201,11 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
             }
 #pragma unroll
             for (int i = 0; i < 2 * MAX_CHUNKS; ++i) pos_cur[i] = pos_next[i];
-            if (qb == 0 && lane == 0)
+            if (qb == 0 && lane == 0 &&
+                SWA_IN_BOUNDS(b < a.B && kvh < a.H_kv && split < a.n_splits, &g_split_err))
                 a.ws_cnt[(static_cast<int64_t>(b) * a.H_kv + kvh) * a.n_splits + split] = count;
-            if (si_new >= 0 && kvh == 0 && qb == 0 && lane == 0)
+            if (si_new >= 0 && kvh == 0 && qb == 0 && lane == 0 &&
+                SWA_IN_BOUNDS(s_new >= 0 && s_new < a.n_slots && b < a.B, &g_split_err))
                 a.slot_pos_w[static_cast<int64_t>(b) * a.n_slots + s_new] = static_cast<int32_t>(t);
             int last_c = -1;
 #pragma unroll
@@ -230,10 +234,11 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
                                                           b * a.k_sb + static_cast<int64_t>(s_new) * a.k_ss + kvh * a.k_sh);
                     uint4 *vd = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(a.v)) +
                                                           b * a.v_sb + static_cast<int64_t>(s_new) * a.v_ss + kvh * a.v_sh);
-                    for (int pc = lane; pc < 2 * (D / 8); pc += 32) {
-                        if (pc < D / 8) kd[pc] = __ldg(ks + pc);
-                        else vd[pc - D / 8] = __ldg(vs + pc - D / 8);
-                    }
+                    if (SWA_IN_BOUNDS(s_new >= 0 && s_new < a.n_slots && b < a.B && kvh < a.H_kv, &g_split_err))
+                        for (int pc = lane; pc < 2 * (D / 8); pc += 32) {
+                            if (pc < D / 8) kd[pc] = __ldg(ks + pc);
+                            else vd[pc - D / 8] = __ldg(vs + pc - D / 8);
+                        }
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     __syncwarp();
                 }
@@ -248,6 +253,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
                         const uint32_t vd = kd + C::STAGE / 2;
                         mbar_arrive_expect_tx(bar_full(st), C::STAGE);
                         const int srow = slot0 + c * CH;
+                        (void)SWA_IN_BOUNDS(srow < a.n_slots, &g_split_err);  // debug build: chunk inside the slots
 #pragma unroll
                         for (int pc = 0; pc < D / 64; ++pc) {
                             tma_load_4d(kd + pc * (CH * 128), &tm_k, bar_full(st), pc * 64, srow, kvh, b);
@@ -306,6 +312,7 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
                         tok = 0;
                     }
                     const int h = kvh * group + r % group;
+                    if (rv[i] && !SWA_IN_BOUNDS(h < a.H_q && b < a.B, &g_split_err)) rv[i] = false;
                     qp[i] = static_cast<const __nv_bfloat16 *>(a.q) + static_cast<int64_t>(b) * a.q_sb + tok * a.q_st +
                             static_cast<int64_t>(h) * a.q_sh;
                 }
@@ -455,6 +462,10 @@ __global__ void __maxnreg__(StreamCfg<D>::CTAS_PER_SM == 3 ? 128 : StreamCfg<D>:
                     const int qs = qb * a.q_per_cta + r / group;
                     bool live = r < rows && qs < a.NQ;
                     if (live && a.q_tok && (a.q_tok[qs] < 0 || a.q_tok[qs] >= a.tok_limit)) live = false;
+                    // debug build: the partial's row (b, query, head, split) exists
+                    if (live && !SWA_IN_BOUNDS(b < a.B && kvh * group + r % group < a.H_q && split < a.n_splits,
+                                               &g_split_err))
+                        live = false;
                     if (live) {
                         const int h = kvh * group + r % group;
                         float mw = -INFINITY;
@@ -549,6 +560,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     const int qs = blockIdx.x / a.H_q, h = blockIdx.x % a.H_q, b = blockIdx.y;
     const int group = a.H_q / a.H_kv, kvh = h / group;
     const int tid = threadIdx.x, ns = a.n_splits;
+    // debug build: the block's row (b, query, head) exists (the grid is NQ * H_q x B)
+    if (!SWA_IN_BOUNDS(qs < a.NQ && h < a.H_q && b < a.B, &g_split_err)) return;
     const int64_t base = ((static_cast<int64_t>(b) * a.NQ + qs) * a.H_q + h) * ns;
     const float2 *ml = reinterpret_cast<const float2 *>(a.ws_ml) + base;  // (max in log2 units, sum)
     if (ns <= kMergeFewSplits) {
