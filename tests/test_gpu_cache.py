@@ -220,3 +220,55 @@ def test_prefill_chunk_full_size_mistral():
     assert (cnt == W).all()
     compare_every_row("mistral chunk (last 4096 tokens)", o.cpu(), lse.cpu().numpy().astype(np.float64), cnt,
                       lambda r: oracle.fwd(q, k, v, W - 1, 0, cfg.scale, rows=r), 1, cfg.Hq, C, t_off=p0)
+
+
+def _decode_workload_on_device():
+    cfg = I.DECODE
+    q, kc, vc, pos, qpos = I.decode_inputs(cfg)
+    return cfg, q, kc, vc, pos, qpos
+
+
+def test_append_full_size():
+    """The appended block of the benchmark: 512 new tokens for each of the 64 decode
+    sequences (after their lengths), into the 4096-slot rings of the decode workload;
+    the whole cache and every slot position compared bit for bit with the oracle."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    cfg, _, kc, vc, pos, qpos = _decode_workload_on_device()
+    L = qpos.astype(np.int64) + 1
+    n_app = 512
+    kn = I.normal_bf16(cfg.seed * 16 + 11, (cfg.B, n_app, cfg.Hkv, cfg.d))
+    vn = I.normal_bf16(cfg.seed * 16 + 12, (cfg.B, n_app, cfg.Hkv, cfg.d))
+    kd, vd, pd = to_dev(kc), to_dev(vc), i32_dev(pos)
+    swa.swa_cache_append(kd, vd, pd, to_dev(kn), to_dev(vn), i32_dev(L.astype(np.int32)))
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    kc2, vc2, pos2 = oracle.cache_append(kc, vc, pos, kn, vn, L.astype(np.int32))
+    np.testing.assert_array_equal(pd.cpu().numpy(), pos2)
+    np.testing.assert_array_equal(_bits(kd), kc2)
+    np.testing.assert_array_equal(_bits(vd), vc2)
+
+
+def test_decode_append_full_size():
+    """Decode with the current token appended in the same pass, on the full decode
+    workload (the benchmark's call): every row against the oracle's decode of the cache
+    with that token appended, and the appended rows and positions bit for bit."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    cfg, q, kc, vc, pos, qpos = _decode_workload_on_device()
+    k1 = I.normal_bf16(cfg.seed * 16 + 13, (cfg.B, cfg.Hkv, cfg.d))
+    v1 = I.normal_bf16(cfg.seed * 16 + 14, (cfg.B, cfg.Hkv, cfg.d))
+    kd, vd, pd = to_dev(kc), to_dev(vc), i32_dev(pos)
+    o, lse, cnt = swa.swa_decode_append(to_dev(q), kd, vd, pd, i32_dev(qpos), to_dev(k1), to_dev(v1), cfg.scale,
+                                        want_counts=True)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    kc2, vc2, pos2 = oracle.cache_append(kc, vc, pos, k1[:, None], v1[:, None], qpos)
+    o_ref, lse_ref, cnt_ref = oracle.decode(q, kc2, vc2, pos2, qpos, cfg.scale)
+    assert_parity(to_host_f64(o), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref, cnt_ref,
+                  "decode with append, full size")
+    np.testing.assert_array_equal(pd.cpu().numpy(), pos2)
+    np.testing.assert_array_equal(_bits(kd), kc2)
+    np.testing.assert_array_equal(_bits(vd), vc2)

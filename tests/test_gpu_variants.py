@@ -265,3 +265,29 @@ def test_gqa_group_16_head_dim_256():
     o, lse, cnt = _run(q, k, v, 50, 0, d ** -0.5)
     o_ref, lse_ref, cnt_ref = oracle.fwd(q, k, v, 50, 0, d ** -0.5)
     assert_parity(o, lse, cnt, o_ref, lse_ref, cnt_ref, "G=16 d=256")
+
+
+def test_decode_sinks_full_size():
+    """The benchmark's decode with four pinned sink slots beside the 4096-slot ring (the
+    decode workload's lengths): every row against the oracle, counts against the closed
+    form min(L, W) + max(0, min(4, L - W))."""
+    import torch
+    import sliding_window_attention_swa_gb300 as swa
+
+    cfg = I.DECODE
+    q, kc, vc, _, qpos = I.decode_inputs(cfg)
+    L = qpos.astype(np.int64) + 1
+    ns = 4
+    pos = I.sink_ring_slot_positions(L, cfg.W, ns)
+    pad = I.normal_bf16(cfg.seed * 16 + 7, (cfg.B, cfg.Hkv, ns, cfg.d))
+    kc = np.concatenate([pad, kc], axis=2)
+    vc = np.concatenate([pad, vc], axis=2)
+    o, lse, cnt = swa.swa_decode(to_dev(q), to_dev(kc), to_dev(vc), i32_dev(pos), i32_dev(qpos), cfg.scale,
+                                 want_counts=True, window=cfg.W, n_sink=ns)
+    torch.cuda.synchronize()
+    swa.swa_check_device_error()
+    o_ref, lse_ref, cnt_ref = oracle.decode(q, kc, vc, pos, qpos, cfg.scale, window=cfg.W, n_sink=ns)
+    assert_parity(to_host_f64(o), lse.cpu().numpy(), cnt.cpu().numpy(), o_ref, lse_ref, cnt_ref,
+                  "decode with 4 sinks, full size")
+    want = np.minimum(L, cfg.W) + np.maximum(0, np.minimum(ns, L - cfg.W))
+    assert (cnt.cpu().numpy() == want[:, None]).all()
