@@ -7,10 +7,11 @@ tensor-core work it did issue, frees its tensor memory and returns.  The host th
 reads SWA_ERR_TIMEOUT with only the wait-expiry bit set (no drain expired), and a
 normal call in the same process still matches the oracle, so the context is usable.
 
-Both producer flavours of the prefill kernel are covered: paired fills (V_j and
-K_{j+1} on one barrier; two query tiles at d = 128 with an odd ring, at d = 64 with
-an even ring, one query tile at d = 256) and one barrier per fill (with global
-positions), and the producer of the decode / global-row split pass.
+The prefill kernel's producer pairs its fills (V_j and K_{j+1} on one barrier); the
+cases cover two query tiles at d = 128 with an odd ring and at d = 64 with an even
+ring, each with and without global positions (whose column tile the producer gathers
+with plain stores), and one query tile at d = 256.  The producer of the decode /
+global-row split pass is covered as well.
 
 Global list: a list that is not strictly increasing within [0, T) is reported as
 SWA_ERR_INVALID_ARG, and the call writes nothing outside its own output buffers.
@@ -54,6 +55,7 @@ BAND = [
     ("paired-d128-odd-ring", (1, 2000, 8, 2, 128, 999, 0), None, 8),
     ("paired-d128-globals", (1, 2000, 8, 2, 128, 999, 0), [0, 1000], 8),
     ("paired-d64-even-ring", (1, 4000, 4, 4, 64, 2000, 0), None, 26),
+    ("paired-d64-globals-short-band", (1, 2000, 4, 4, 64, 256, 256), [0, 1000], 10),
     ("paired-d256-one-tile", (1, 1500, 2, 1, 256, 1000, 0), None, 12),
     ("paired-d128-first-fill", (1, 700, 4, 2, 128, 300, 0), None, 0),
 ]
