@@ -14,8 +14,9 @@
 // (prathamp.com "Sliding Window Attention: From Local Windows to Global Context",
 // section 4.3).
 //
-// Persistent: one CTA per SM walks the units (longest first, round-robin); TMEM and
-// the mbarriers are set up once and every barrier phase runs on across units.
+// Persistent: one CTA per SM walks the units (longest first, dealt in rounds of the grid
+// size in alternating directions); TMEM and the mbarriers are set up once and every
+// barrier phase runs on across units.
 // Roles:
 //   warp 0        K/V producer: K_0, V_0, K_1, V_1, ... of every unit into a ring of
 //                 NSLOT shared-memory slots (TMA for band tiles, plain gathers into
@@ -244,10 +245,18 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         const int n = NSLOT % 2 == 1 ? (i - (sl & 1) + 1) / 2 : (sl % 2 == 0 ? i : 0);
         return static_cast<uint32_t>(n & 1);
     };
+    // This CTA's i-th unit.  Units are numbered longest first and dealt in rounds of
+    // gridDim.x, in alternating directions (a CTA that takes a round's longest unit takes
+    // the next round's shortest), so the per-CTA totals of the shorter units at the end
+    // even out.
+    auto unit_at = [&](int i) -> int {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        return i * G + ((i & 1) ? G - 1 - c : c);
+    };
     // key tiles of this CTA over all its units: ring fills 0 .. 2 * count - 1
     auto count_cta_tiles = [&]() -> int {
         int c = 0;
-        for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) c += unit_of<NQT, BN>(u, a).n_tiles;
+        for (int i = 0; unit_at(i) < a.n_units; ++i) c += unit_of<NQT, BN>(unit_at(i), a).n_tiles;
         return c;
     };
     auto kpar = [&](int p) -> uint32_t {
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             __syncwarp();
         };
         const int cta_tiles = count_cta_tiles(), nfill = 2 * cta_tiles;
-        int u = blockIdx.x, j = 0;
+        int ui = 0, u = unit_at(0), j = 0;  // unit ordinal, unit, tile within it
         Unit w{};
         if (u < a.n_units) w = unit_of<NQT, BN>(u, a);
         // planted fault: only the steps whose fills all lie below a.fault_stop_fill run
@@ -413,9 +422,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
         for (int t = 0; t < n_steps; ++t) {
             // the tile after (u, j), possibly the next unit's first
-            int u2 = u, j2 = j + 1;
+            int u2 = u, j2 = j + 1, ui2 = ui;
             if (j2 >= w.n_tiles) {
-                u2 = u + static_cast<int>(gridDim.x);
+                ui2 = ui + 1;
+                u2 = unit_at(ui2);
                 j2 = 0;
             }
             const bool has_next = t + 1 < cta_tiles;
@@ -428,6 +438,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             fill(w, j, true, pv % NSLOT, has_next, w2, j2, own % NSLOT, bar_full(own % NSLOT));
             g = own + 1;
             u = u2;
+            ui = ui2;
             j = j2;
             w = w2;
         }
@@ -448,7 +459,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         int issued[2] = {0, 0};  // query loads issued per tile
         bool ok = true;
 #pragma unroll 1
-        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+        for (int u = unit_at(0); u < a.n_units && ok; ++k, u = unit_at(k)) {
             const Unit w = unit_of<NQT, BN>(u, a);
 #pragma unroll 1
             for (int x = 0; x < NQT && ok; ++x) {
@@ -535,7 +546,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             auto kslot = [&](int jg) { return (2 * jg) % NSLOT; };
             auto vslot = [&](int jg) { return (2 * jg + 1) % NSLOT; };
 #pragma unroll 1
-            for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+            for (int u = unit_at(0); u < a.n_units && ok; ++k, u = unit_at(k)) {
                 const int n = unit_of<NQT, BN>(u, a).n_tiles;
                 // tile jj of the unit is the narrow global-column tile
                 const int nb = kGlob ? unit_of<NQT, BN>(u, a).n_band : n;
@@ -620,7 +631,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         bool ok = true;
         int J = 0, k = 0;
 #pragma unroll 1
-        for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x, ++k) {
+        for (int u = unit_at(0); u < a.n_units && ok; ++k, u = unit_at(k)) {
             const Unit w = unit_of<NQT, BN>(u, a);
             const int tx = w.t0 + wg * a.TQ;  // first token of this warpgroup's query tile
             const int t = tx + tq;
