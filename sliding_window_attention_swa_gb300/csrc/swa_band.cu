@@ -31,8 +31,9 @@
 //   warp 1        TMEM owner and MMA issuer (one thread):
 //                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
-//   warp 2        Q loader: a unit's query tiles once every MMA of the previous unit
-//                 has completed (its S MMAs were the last to read that shared memory).
+//   warp 2        Q loader: a unit's query tiles once the previous unit's last S MMA
+//                 from that tile has completed (its only readers; with global positions,
+//                 once the previous unit's epilogue has seen all its MMAs complete).
 //   softmax WGs   NQT warpgroups; one row per thread (TMEM lane).  Scores are masked
 //                 only on band-edge and global tiles; the running max is kept in the
 //                 log2 domain; P = 2^(x - m) is written back as bf16 over the S
@@ -656,6 +657,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     ok = false;
                     break;
                 }
+                // Without global positions the query tile is released here, at the unit's
+                // last S MMA from it (its only readers), so the next unit's rows load while
+                // this tile's last softmax, P V and epilogue run: Mistral +0.9% in an A/B.
+                // The builds with global positions release it after the epilogue: there the
+                // early release measured 4-7% slower (Longformer, Mistral with sinks).
+                if (!kGlob && j + 1 == w.n_tiles && lane == 0) mbar_arrive(bar_qe(wg));
                 if constexpr (kSoftRel) {
                     // S_B(jg) was the last MMA issued before this commit: every reader of
                     // K_jg (and of V_{jg-1}) is done, so the key fill's slot is released here
@@ -967,7 +974,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             }
             tc_fence_after();
             // every MMA of this unit has completed: the Q loader may refill this tile
-            if (lane == 0) mbar_arrive(bar_qe(wg));
+            if (kGlob && lane == 0) mbar_arrive(bar_qe(wg));
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = a.o + static_cast<int64_t>(w.b) * a.o_st[0] + static_cast<int64_t>(t) * a.o_st[1] +
                                   static_cast<int64_t>(h) * a.o_st[2];
