@@ -355,6 +355,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
+// The descriptor of the same matrix layout starting `bytes` (a multiple of 16) further:
+// the start address field holds bits 4-17 of a shared-memory address, so for any address
+// below 256 KB the offset is one addition that never carries out of the field.
+__device__ __forceinline__ uint64_t desc_offset(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 (PTX ISA, "Instruction descriptor"):
 // D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9 = 1, 10-12 = 1), A / B major-ness
 // (bit 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in 24-28.

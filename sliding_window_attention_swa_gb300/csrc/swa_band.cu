@@ -511,10 +511,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
+                // one descriptor per operand; a K slice is a constant byte offset from it
+                const uint64_t a0 = smem_desc(qb, 16, 1024, kSwizzle128B), b0 = smem_desc(kb, 16, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = smem_desc(qb + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(kb + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t ad = desc_offset(a0, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+                    const uint64_t bd = desc_offset(b0, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
                     uint32_t id = idS;
                     if constexpr (kGlob) id = narrow ? idS_narrow : idS;
                     tc_mma_ss(tmem + C::tm_s(slot), ad, bd, id, kk > 0 ? 1u : 0u);
@@ -533,12 +535,13 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (first && k >= 1 && !mbar_wait(bar_of(otile), (k - 1) & 1, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t vb = sRing + s * C::TBYTES;
+                const uint64_t v0 = smem_desc(vb, BN * 128, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     if constexpr (kGlob) {
                         if (narrow && kk >= kNarrow / 16) break;
                     }
-                    const uint64_t bd = smem_desc(vb + kk * 2048, BN * 128, 1024, kSwizzle128B);
+                    const uint64_t bd = desc_offset(v0, kk * 2048);
                     tc_mma_ts(tmem + C::tm_o(otile), tmem + C::tm_s(slot) + kk * 8, bd, idPV,
                               (!first || kk > 0) ? 1u : 0u);
                 }
