@@ -503,6 +503,20 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             int cta_tiles = 0;
             cta_tiles = count_cta_tiles();
             // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
+            // The query tiles never move: at head dim 128 the A descriptor of every K slice of
+            // each is built once here, a constant of the CTA, since the MMA thread's instruction
+            // count per tile is part of the tile period (Mistral +1.3% in an A/B).  At 64 the
+            // same cost the Longformer shape 0.9% and at 256 it changed nothing: there each
+            // descriptor is an offset from the tile's.
+            constexpr bool kQDesc = D == 128;
+            uint64_t qdesc[NQT][D / 16];
+#pragma unroll
+            for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    qdesc[qt][kk] = kQDesc ? smem_desc(sQ + qt * C::QBYTES + (kk >> 2) * (BM * 128) + (kk & 3) * 32,
+                                                       16, 1024, kSwizzle128B)
+                                           : 0ull;
             auto mma_s = [&](int slot, int qt, int jg, bool wait_k, bool narrow = false) -> bool {
                 const int fi = 2 * jg, s = fi % NSLOT;
                 // paired fills: a key fill owns its barrier (with V_{jg-1} on it); with two
@@ -511,11 +525,12 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (wait_k && !mbar_wait(bar_full(s), kpty, abort, &g_band_err)) return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + qt * C::QBYTES, kb = sRing + s * C::TBYTES;
-                // one descriptor per operand; a K slice is a constant byte offset from it
+                // one descriptor per operand tile; a K slice is a constant byte offset from it
                 const uint64_t a0 = smem_desc(qb, 16, 1024, kSwizzle128B), b0 = smem_desc(kb, 16, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = desc_offset(a0, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+                    const uint64_t ad =
+                        kQDesc ? qdesc[qt][kk] : desc_offset(a0, (kk >> 2) * (BM * 128) + (kk & 3) * 32);
                     const uint64_t bd = desc_offset(b0, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
                     uint32_t id = idS;
                     if constexpr (kGlob) id = narrow ? idS_narrow : idS;
