@@ -517,6 +517,19 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     qdesc[qt][kk] = kQDesc ? smem_desc(sQ + qt * C::QBYTES + (kk >> 2) * (BM * 128) + (kk & 3) * 32,
                                                        16, 1024, kSwizzle128B)
                                            : 0ull;
+            // The V slice descriptors of value tile jg: with two query tiles both P V of a tile
+            // step read one V tile, so the set is built once per tile step (Mistral +2.7%,
+            // Mistral with sinks +1.3%, the Longformer shape without globals +1.2% in an A/B;
+            // not in the head-dim-64 build with global positions, where it measured 1.1%
+            // slower).  Sharing the K slice descriptors of the two S MMAs as well made the
+            // head-dim-128 MMA thread spill and ran slower.
+            constexpr bool kShareV = NQT == 2 && (D == 128 || !kGlob);
+            uint64_t vd[BN / 16];
+            auto v_descs = [&](int jg) {
+                const uint64_t v0 = smem_desc(sRing + ((2 * jg + 1) % NSLOT) * C::TBYTES, BN * 128, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) vd[kk] = desc_offset(v0, kk * 2048);
+            };
             auto mma_s = [&](int slot, int qt, int jg, bool wait_k, bool narrow = false) -> bool {
                 const int fi = 2 * jg, s = fi % NSLOT;
                 // paired fills: a key fill owns its barrier (with V_{jg-1} on it); with two
@@ -540,7 +553,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             };
             // O_tile (+)= P(slot) V of global tile index jg; `first` starts a fresh O.
             auto mma_pv = [&](int slot, int otile, int jg, uint32_t p_parity, bool wait_v, bool first,
-                              bool narrow = false) -> bool {
+                              bool narrow = false, bool have_vd = false) -> bool {
                 const int fi = 2 * jg + 1, s = fi % NSLOT;
                 if (!mbar_wait(bar_pf(slot), p_parity, abort, &g_band_err)) return false;
                 // V_jg arrives on the barrier of the key fill after it (K_{jg+1}), if any
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     if constexpr (kGlob) {
                         if (narrow && kk >= kNarrow / 16) break;
                     }
-                    const uint64_t bd = desc_offset(v0, kk * 2048);
+                    const uint64_t bd = have_vd ? vd[kk] : desc_offset(v0, kk * 2048);
                     tc_mma_ts(tmem + C::tm_o(otile), tmem + C::tm_s(slot) + kk * 8, bd, idPV,
                               (!first || kk > 0) ? 1u : 0u);
                 }
@@ -588,7 +601,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
 #pragma unroll 1
                     for (int j = 0; j < n && ok; ++j) {
                         const int jg = J + j;
-                        ok = mma_pv(0, 0, jg, jg & 1, true, j == 0, narrow(j));
+                        if constexpr (kShareV) v_descs(jg);
+                        ok = mma_pv(0, 0, jg, jg & 1, true, j == 0, narrow(j), kShareV);
                         if (!ok) break;
                         if (j + 1 < n) {
                             ok = mma_s(0, 0, jg + 1, false, narrow(j + 1));
@@ -597,7 +611,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         } else {
                             tc_commit(bar_od(0));
                         }
-                        ok = mma_pv(1, 1, jg, jg & 1, false, j == 0, narrow(j));
+                        ok = mma_pv(1, 1, jg, jg & 1, false, j == 0, narrow(j), kShareV);
                         if (!ok) break;
                         if constexpr (!kKeyRel) tc_commit(bar_empty(vslot(jg)));
                         if (j + 1 < n) {
