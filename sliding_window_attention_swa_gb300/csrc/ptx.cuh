@@ -314,6 +314,11 @@ __device__ __forceinline__ void tc_mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void tc_cp_128x256b_e(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr), "l"(s_desc)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_commit_e(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"

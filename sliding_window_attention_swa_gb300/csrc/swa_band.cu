@@ -108,8 +108,17 @@ struct BandCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     __host__ __device__ static constexpr uint32_t tm_s(int slot) { return static_cast<uint32_t>(slot * BN); }
     __host__ __device__ static constexpr uint32_t tm_o(int tile) { return 256u + static_cast<uint32_t>(tile * 128); }
+    // One query tile (head dim 256): the tile is copied into tensor memory once per unit
+    // (sixteen tcgen05.cp of 128 rows x 256 bits, issued in order by the MMA warp, which then
+    // releases the tile's shared memory with one commit) into the 128 columns between
+    // S0 | S1 and O, and every S MMA takes its A operand from there, reading only its K slice
+    // from shared memory (2 KB instead of 6 KB per 128x64x16 MMA): Gemma-local 1138 -> 1198
+    // TFLOP/s in an A/B.
+    static constexpr bool QTM = NQT == 1;
+    static constexpr uint32_t TM_Q = 128;
     static_assert(NSLOT >= 3, "K/V ring too shallow");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(!QTM || (tm_s(1) + BN <= TM_Q && TM_Q + D / 2 <= tm_o(0)), "query tile in tensor memory");
     static_assert(tm_o(NQT - 1) + D <= TMEM_COLS && tm_s(1) + BN <= 256, "tensor memory budget");
 };
 
@@ -289,7 +298,9 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
         abort_flag = 0;
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar_qf(x), 1);
-            mbar_init(bar_qe(x), 4);  // the four warps of the tile's softmax warpgroup
+            // the four warps of the tile's softmax warpgroup; with the tile in tensor memory,
+            // the MMA warp's one commit after the copy
+            mbar_init(bar_qe(x), C::QTM ? 1 : 4);
             mbar_init(bar_sf(x), 1);
             mbar_init(bar_pf(x), 4);
             mbar_init(bar_od(x), 1);
@@ -509,12 +520,11 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             int cta_tiles = 0;
             cta_tiles = count_cta_tiles();
             // S into TMEM slot `slot` from query tile `qt` and the K tile of global tile index jg.
-            // The query tiles never move: at head dim 128 the A descriptor of every K slice of
-            // each is built once here, a constant of the CTA, since the MMA thread's instruction
-            // count per tile is part of the tile period (Mistral +1.3% in an A/B).  At 64 the
-            // same cost the Longformer shape 0.9% and at 256 it changed nothing: there each
-            // descriptor is an offset from the tile's.
-            constexpr bool kQDesc = D == 128;
+            // The query tiles never move: the A descriptor of every K slice of each is built once
+            // here, a constant of the CTA, since the MMA warp's instruction count per tile is
+            // part of the tile period (Mistral +1.3%, Longformer +1.7% in A/B runs).  With the
+            // query tile in tensor memory (one query tile) the S MMAs take no A descriptor.
+            constexpr bool kQDesc = !C::QTM;
             uint64_t qdesc[NQT][D / 16];
 #pragma unroll
             for (int qt = 0; qt < NQT; ++qt)
@@ -525,11 +535,10 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                                            : 0ull;
             // The V slice descriptors of value tile jg: with two query tiles both P V of a tile
             // step read one V tile, so the set is built once per tile step (Mistral +2.7%,
-            // Mistral with sinks +1.3%, the Longformer shape without globals +1.2% in an A/B;
-            // not in the head-dim-64 build with global positions, where it measured 1.1%
-            // slower).  Sharing the K slice descriptors of the two S MMAs as well made the
-            // head-dim-128 MMA thread spill and ran slower.
-            constexpr bool kShareV = NQT == 2 && (D == 128 || !kGlob);
+            // Mistral with sinks +1.3%, the Longformer shape without globals +1.2% in an A/B).
+            // Sharing the K slice descriptors of the two S MMAs as well made the head-dim-128
+            // MMA warp spill and ran slower.
+            constexpr bool kShareV = NQT == 2;
             uint64_t vd[BN / 16];
             auto v_descs = [&](int jg) {
                 const uint64_t v0 = smem_desc(sRing + ((2 * jg + 1) % NSLOT) * C::TBYTES, BN * 128, 1024, kSwizzle128B);
@@ -553,7 +562,8 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                     const uint64_t bd = desc_offset(b0, (kk >> 2) * (BN * 128) + (kk & 3) * 32);
                     uint32_t id = idS;
                     if constexpr (kGlob) id = narrow ? idS_narrow : idS;
-                    tc_mma_ss_e(tmem + C::tm_s(slot), ad, bd, id, kk > 0 ? 1u : 0u);
+                    if constexpr (C::QTM) tc_mma_ts_e(tmem + C::tm_s(slot), tmem + C::TM_Q + kk * 8, bd, id, kk > 0 ? 1u : 0u);
+                    else tc_mma_ss_e(tmem + C::tm_s(slot), ad, bd, id, kk > 0 ? 1u : 0u);
                 }
                 return true;
             };
@@ -630,6 +640,17 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                         }
                     }
                 } else {
+                    if constexpr (C::QTM) {
+                        // the unit's query tile into tensor memory, 16 columns per copy (the
+                        // previous unit's last S MMA precedes the copies in the tensor pipe);
+                        // its shared memory is free for the next unit once they complete
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            tc_cp_128x256b_e(tmem + C::TM_Q + kk * 8,
+                                             smem_desc(sQ + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B));
+                        tc_commit_e(bar_qe(0));
+                    }
                     ok = mma_s(J & 1, 0, J, true, narrow(0));
                     if (ok) {
                         tc_commit_e(bar_sf(J & 1));
@@ -700,7 +721,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 // this tile's last softmax, P V and epilogue run: Mistral +0.9% in an A/B.
                 // The builds with global positions release it after the epilogue: there the
                 // early release measured 4-7% slower (Longformer, Mistral with sinks).
-                if (!kGlob && j + 1 == w.n_tiles && lane == 0) mbar_arrive(bar_qe(wg));
+                if (!kGlob && !C::QTM && j + 1 == w.n_tiles && lane == 0) mbar_arrive(bar_qe(wg));
                 if constexpr (kSoftRel) {
                     // S_B(jg) was the last MMA issued before this commit: every reader of
                     // K_jg (and of V_{jg-1}) is done, so the key fill's slot is released here
@@ -1012,7 +1033,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
             }
             tc_fence_after();
             // every MMA of this unit has completed: the Q loader may refill this tile
-            if (kGlob && lane == 0) mbar_arrive(bar_qe(wg));
+            if (kGlob && !C::QTM && lane == 0) mbar_arrive(bar_qe(wg));
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = a.o + static_cast<int64_t>(w.b) * a.o_st[0] + static_cast<int64_t>(t) * a.o_st[1] +
                                   static_cast<int64_t>(h) * a.o_st[2];
