@@ -22,14 +22,15 @@
 //                 NSLOT shared-memory slots (TMA for band tiles, plain gathers into
 //                 the same 128B-swizzled layout for global tiles).  V_j and K_{j+1} are
 //                 copied together and signal one barrier (that of K_{j+1}'s slot): with
-//                 two query tiles the issuing thread then waits once per key tile, before
+//                 two query tiles the MMA warp then waits once per key tile, before
 //                 P_A V_j, and S_A(j+1) needs no wait of its own; with one query tile the
 //                 wait before S(j+1) covers V_j's P V.  With two query tiles, ring slots
 //                 are released by key fills (a value fill's last reader precedes the next
 //                 key fill's); without global positions that release is an arrive by
 //                 softmax warpgroup B once it sees S_B(j) done.
 //   warp 1        TMEM owner and MMA issuer (warp-uniform loop, one elected lane issues):
-//                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory)
+//                   S_X   = Q_X K_j^T   (tcgen05.mma, A/B from shared memory; at head dim
+//                                        256 A = Q from tensor memory)
 //                   O_X  += P_X V_j     (tcgen05.mma, A = P from tensor memory)
 //   warp 2        Q loader: a unit's query tiles once the previous unit's last S MMA
 //                 from that tile has completed (its only readers; with global positions,
@@ -43,7 +44,7 @@
 //                 stored straight from registers; lse and attended-key counts.
 // NQT = 2 (head dim <= 128): two query tiles ping-pong -- while one warpgroup turns
 // S_A into P_A the tensor cores run S_B and P_B V -- with TMEM S_A | S_B | O_A | O_B.
-// NQT = 1 (head dim 256): one query tile, S double-buffered, TMEM S0 | S1 | O.
+// NQT = 1 (head dim 256): one query tile, S double-buffered, TMEM S0 | S1 | Q | O.
 // Builds per head dim: with and without global-position code (kGlob), and for long and
 // short bands (kShort: at most kShortTiles key tiles per unit, where most tiles are band
 // edges or lie beyond one query tile's band).  At most kNarrow global positions take one
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     // producer warp: its part of a pair is counted by one plain arrival once its stores are
     // visible to the async proxy, the TMA part by expected bytes.
     // kSoftRel (no global positions, two query tiles): softmax warpgroup B, which waits for
-    // S_B(j) anyway, releases K_j's slot instead of a commit on the issuing thread
+    // S_B(j) anyway, releases K_j's slot instead of a commit by the MMA warp
     constexpr bool kSoftRel = !kGlob && NQT == 2;
     auto fpar = [&](int q) -> uint32_t {
         const int sl = q % NSLOT, i = q / NSLOT;
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
     } else if (warp == 1) {
         // ============================ MMA issuer ============================
         if constexpr (NQT == 2) regs_dec<C::REG_CTRL>();
-        // Every lane of the warp runs the MMA thread's loop, so its control flow and the
+        // Every lane of the warp runs the MMA issuer's loop, so its control flow and the
         // descriptor and index arithmetic stay warp-uniform; inside each tcgen05 instruction's
         // asm, elect.sync picks the one lane that issues it (always the same lane, so each
         // commit tracks all MMAs before it).  The same loop run by lane 0 alone, in a
@@ -725,7 +726,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if constexpr (kSoftRel) {
                     // S_B(jg) was the last MMA issued before this commit: every reader of
                     // K_jg (and of V_{jg-1}) is done, so the key fill's slot is released here
-                    // rather than by another commit on the issuing thread
+                    // rather than by another commit of the MMA warp
                     if (wg == 1 && quarter == 0 && lane == 0) mbar_arrive(bar_empty((2 * jg) % NSLOT));
                 }
                 tc_fence_after();
@@ -971,7 +972,7 @@ __global__ void __launch_bounds__(BandCfg<D>::THREADS, 1)
                 if (__any_sync(0xffffffffu, need) && j > 0) {
                     // O holds P V of tiles 0 .. j-1 of this unit and must be complete: the
                     // release of tile j-1's V slot (fill 2(j-1)+1) is committed right after
-                    // that P V (no commit of its own on the issuing thread)
+                    // that P V (no commit of its own by the MMA warp)
                     if constexpr (NQT == 1) {
                         if (!warp_wait(bar_empty((2 * (jg - 1) + 1) % NSLOT), vpar(2 * (jg - 1) + 1),
                                        abort)) {
